@@ -1,0 +1,168 @@
+"""Pins of the oracle's expert FFN and combine: a brute-force per-token
+restatement, a dense special case recomputed with torch library routines,
+the identical-experts identity, and the pages' 0.73/0.27 combine example."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_layer_counts_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(x_bf16: torch.Tensor) -> np.ndarray:
+    return x_bf16.view(torch.int16).numpy().astype(np.uint16)
+
+
+def _small(T, H, I, E, k, seed=0):
+    w = inputs.Workload("t", T, H, I, E, k, "uniform")
+    d = inputs.make_inputs(w, seed=seed)
+    return w, d
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(8, 64, 32, 4, 2), (64, 256, 128, 8, 2)])
+def test_bruteforce_matches_pool_oracle(oracle, T, H, I, E, k):
+    w, d = _small(T, H, I, E, k)
+    x = _bits(d["x"])
+    idx = d["topk_idx"].numpy()
+    tw = d["topk_w"].numpy()
+    args = [a.numpy() for a in (d["w1q"], d["w1sf"], d["w2q"], d["w2sf"])]
+    res = oracle.forward(x, idx, tw, E, *args)
+    assert res["status"] == 0
+    for t in range(T):
+        yb, st = oracle.bruteforce_token(x[t], idx[t], tw[t], E, *args)
+        assert st == 0
+        np.testing.assert_array_equal(yb, res["y"][t])
+    # a token subset gives the same rows
+    sub = np.array([5, 0, T - 1], np.int32)
+    rs = oracle.forward(x, idx, tw, E, *args, tokens=sub)
+    np.testing.assert_array_equal(rs["y"], res["y"][sub])
+
+
+def _ue8m0(a, m):
+    if a == 0:
+        return 0
+    e = math.ceil(math.log2(a / m))
+    while a > m * 2.0 ** e:
+        e += 1
+    while a <= m * 2.0 ** (e - 1):
+        e -= 1
+    return max(-126, min(127, e))
+
+
+def _golden_e2m1():
+    vals = {}
+    with open(os.path.join(GOLDEN, "e2m1_values.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                c, v = line.split()
+                vals[int(c, 16)] = float(v)
+    return torch.tensor([vals[i] for i in range(16)], dtype=torch.float64)
+
+
+def _deq_w(q, sf, tab):
+    lo = (q & 15).long()
+    hi = (q >> 4).long()
+    nib = torch.stack([lo, hi], dim=-1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    v = tab[nib]
+    s = torch.exp2(sf.double() - 127).repeat_interleave(32, dim=-1)
+    return v * s
+
+
+def _mx8_torch(v64: torch.Tensor):
+    """MXFP8 with torch's E4M3 cast: returns dequantised float64."""
+    rows = v64.reshape(-1, 32)
+    out = torch.empty_like(rows)
+    for i in range(rows.shape[0]):
+        e = _ue8m0(float(rows[i].abs().max()), 448.0)
+        codes = (rows[i] * 2.0 ** -e).to(torch.float32).to(torch.float8_e4m3fn)
+        out[i] = codes.to(torch.float64) * 2.0 ** e
+    return out.reshape(v64.shape)
+
+
+def test_dense_special_case_against_torch(oracle):
+    """E=1, k=1, w=1: the layer is a dense quantised FFN; recompute it with
+    torch matmuls and torch's E4M3/bf16 casts."""
+    T, H, I = 16, 128, 64
+    w, d = _small(T, H, I, 1, 1, seed=3)
+    idx = np.zeros((T, 1), np.int64)
+    tw = np.ones((T, 1), np.float32)
+    args = [a.numpy() for a in (d["w1q"], d["w1sf"], d["w2q"], d["w2sf"])]
+    y = oracle.forward(_bits(d["x"]), idx, tw, 1, *args)["y"]
+
+    tab = _golden_e2m1()
+    W1 = _deq_w(d["w1q"][0], d["w1sf"][0], tab)  # [2I, H]
+    W2 = _deq_w(d["w2q"][0], d["w2sf"][0], tab)  # [H, I]
+    xq = _mx8_torch(d["x"].to(torch.float64))
+    acc = (xq @ W1.T).to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    g, u = acc[:, :I], acc[:, I:]
+    silu = (g / (1.0 + torch.exp(-g))).to(torch.float32)
+    h = (silu * u.to(torch.float32)) * 1.0
+    hq = _mx8_torch(h.to(torch.float64))
+    o = (hq @ W2.T).to(torch.float32).to(torch.bfloat16)
+    ref = o.view(torch.int16).numpy().astype(np.uint16)
+    mism = np.mean(ref != y)
+    assert mism <= 1e-3, mism
+    yf = torch.from_numpy(y.astype(np.int16)).view(torch.bfloat16).double()
+    assert torch.linalg.norm(yf - o.double()) <= 1e-3 * torch.linalg.norm(o.double())
+
+
+def test_identical_experts_identity(oracle):
+    """E identical experts with power-of-two weights: y = bf16((sum w) * FFN(x)),
+    exactly (UE8M0 requant is invariant to power-of-two scaling)."""
+    T, H, I, E, k = 32, 128, 64, 4, 3
+    w, d = _small(T, H, I, 1, 1, seed=5)
+    rep = lambda a: np.repeat(a.numpy(), E, axis=0)
+    args = [rep(d[n]) for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    one = [d[n].numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    rng = np.random.default_rng(0)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int64)
+    tw = np.array([[0.5, 0.25, 0.125]] * T, np.float32)
+    x = _bits(d["x"])
+    y = oracle.forward(x, idx, tw, E, *args)["y"]
+    o1 = oracle.forward(x, np.zeros((T, 1), np.int64), np.ones((T, 1), np.float32), 1, *one)["y"]
+    o1f = torch.from_numpy(o1.astype(np.int16)).view(torch.bfloat16).double()
+    ref = (0.875 * o1f).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    np.testing.assert_array_equal(y, ref)
+
+
+def test_combine_example_semantics(oracle):
+    """Output(T0) = 0.73 * Expert2(T0) + 0.27 * Expert7(T0) (golden example)."""
+    rows = []
+    with open(os.path.join(GOLDEN, "combine_example.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                t, e, wt = line.split()
+                rows.append((int(e), float(wt)))
+    (e_a, w_a), (e_b, w_b) = rows
+    T, H, I, E = 16, 256, 128, 8
+    w, d = _small(T, H, I, E, 2, seed=7)
+    args = [d[n].numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    x = _bits(d["x"])
+    idx = np.array([[e_a, e_b]] * T, np.int64)
+    tw = np.array([[w_a, w_b]] * T, np.float32)
+    y = oracle.forward(x, idx, tw, E, *args)["y"]
+    ya = oracle.forward(x, np.full((T, 1), e_a, np.int64), np.ones((T, 1), np.float32), E, *args)["y"]
+    yb = oracle.forward(x, np.full((T, 1), e_b, np.int64), np.ones((T, 1), np.float32), E, *args)["y"]
+    f = lambda a: torch.from_numpy(a.astype(np.int16)).view(torch.bfloat16).double()
+    ref = w_a * f(ya) + w_b * f(yb)
+    swapped = w_b * f(ya) + w_a * f(yb)
+    err = torch.linalg.norm(f(y) - ref) / torch.linalg.norm(ref)
+    err_sw = torch.linalg.norm(f(y) - swapped) / torch.linalg.norm(ref)
+    assert err < 0.1, err
+    assert err_sw > 0.3, err_sw
+
+
+def test_tokens_without_valid_entry_are_zero(oracle):
+    T, H, I, E = 8, 64, 32, 4
+    w, d = _small(T, H, I, E, 2, seed=9)
+    args = [d[n].numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    idx = d["topk_idx"].numpy().copy()
+    idx[3] = -1
+    idx[5, 0] = -1
+    y = oracle.forward(_bits(d["x"]), idx, d["topk_w"].numpy(), E, *args)["y"]
+    assert np.all(y[3] == 0)
+    assert np.any(y[5] != 0)
