@@ -1,0 +1,330 @@
+"""Benchmark of the fused MoE layer forward on GB300.
+
+One step = the whole hot path on one batch: moe_plan (route_count,
+route_scan, route_slot) + moe_forward (dispatch_quant, expert L1, expert L2,
+combine), on the full skewed workload T=8192, H=7168, I=2048, E=256, k=8 by
+default.  Inputs are synthetic and seeded, resident in HBM before timing;
+L2 is flushed (a 512 MB buffer is written) before every timed step, outside
+the timed events.  FLOPs = 6 * N * H * I with N the number of valid top-k
+entries.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload full]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+With N > 1 (torchrun), each rank runs an independent replica of the layer on
+its own GPU (the layer does not shard on one node: weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_layer_counts_gb300 import inputs  # noqa: E402
+
+METRIC = "MoE fwd TFLOP/s & tokens/s (T=8192,H=7168,I=2048,E=256,k=8); % FP8 peak"
+STAGES = ("route", "dispatch", "expert_l1", "expert_l2", "combine")
+KERNELS_PER_STEP = 7  # route_count, route_scan, route_slot, dispatch_quant, L1, L2, combine
+FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    """Roofline denominators: measured copy bandwidth and bf16 GEMM rate of
+    this GPU pool; FP8 (the MXF8F6F4 rate) taken as 2x the bf16 rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        m = json.load(open(path))
+        return dict(hbm_gbs=m["hbm_gbs"], bf16=m["bf16_tflops"], bf16_sus=m["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.samples = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) == 7:
+                try:
+                    self.samples.append((float(f[0]), float(f[1]), f[3:]))
+                except ValueError:
+                    pass
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, r in self.samples for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": max(s[1] for s in self.samples),
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "moe_expert_layer_counts_gb300", "csrc", "expert_gemm.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def measured_traffic():
+    """Per-launch DRAM bytes of the L1 kernel on this workload from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "expert_l1_traffic.json")
+    if not os.path.exists(path):
+        return None
+    m = json.load(open(path))
+    return m.get("bytes_per_launch") if m.get("kernel_sha") == kernel_source_hash() else None
+
+
+def cpu_baseline(w, d, n_tokens: int):
+    """The oracle, as it stands, on the host cores: a bounded sample of tokens."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    x = d["x"].cpu().view(torch.int16).numpy().view(np.uint16)
+    idx = d["topk_idx"].cpu().numpy()
+    tw = d["topk_w"].cpu().numpy()
+    ws = [d[n].cpu().numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    step = max(1, w.T // n_tokens)
+    toks = np.arange(0, w.T, step, dtype=np.int32)[:n_tokens]
+    t0 = time.perf_counter()
+    oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
+    dt = time.perf_counter() - t0
+    n_valid = int((idx[toks] >= 0).sum())
+    return dict(value=6.0 * n_valid * w.H * w.I / dt / 1e12, unit="TFLOP/s", cores=oracle.num_threads(),
+                kind="oracle", seconds=dt, tokens_per_s=len(toks) / dt,
+                sample=f"{len(toks)} tokens (every {step}th) of the {w.name} workload, {n_valid} valid entries, "
+                       f"weights dequantised per touched expert inside the timing")
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the CPU oracle timed as it stands; rank 0 only."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    d = inputs.make_inputs(w, device="cpu", weight_device="cuda" if torch.cuda.is_available() else "cpu")
+    x = d["x"].view(torch.int16).numpy().view(np.uint16)
+    idx = d["topk_idx"].numpy()
+    tw = d["topk_w"].numpy()
+    ws = [d[n].cpu().numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    per_step = max(1, args.ref_tokens)
+    times, flops = [], 0.0
+    for s in range(args.warmup + args.steps):
+        toks = np.unique((np.arange(per_step, dtype=np.int64) * 977 + s * 131) % w.T).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            flops += 6.0 * int((idx[toks] >= 0).sum()) * w.H * w.I
+    total = sum(times)
+    value = flops / total / 1e12
+    line = dict(metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=1e3 * total / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}",
+                            sample=f"{per_step} tokens per step"),
+                cpu_baseline=dict(value=value, unit="TFLOP/s", cores=oracle.num_threads(), kind="oracle",
+                                  sample=f"{per_step} tokens per step of the {w.name} workload"),
+                e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="full", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=1, help="oracle tokens per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    w = inputs.WORKLOADS[args.workload]
+    rank, world = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import moe_expert_layer_counts_gb300 as moe
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = inputs.make_inputs(w, seed=0, device=dev)
+    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"])
+    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"])
+    ws = moe.alloc_workspace(w.T, w.k, w.E, w.H, w.I, dev)
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_valid = int((d["topk_idx"] >= 0).sum().item())
+    flops = 6.0 * n_valid * w.H * w.I
+
+    def step(ev=None):
+        if ev: ev[0].record()
+        p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I, workspace=ws)
+        if ev: ev[1].record()
+        moe.dispatch(p, d["x"])
+        if ev: ev[2].record()
+        moe.expert_l1(p, W1)
+        if ev: ev[3].record()
+        moe.expert_l2(p, W2)
+        if ev: ev[4].record()
+        moe.combine(p, y)
+        if ev: ev[5].record()
+        return p
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        p = step()
+    torch.cuda.synchronize()
+    status = moe.plan_check(p)
+    assert status == 0, moe.error_string(status)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 255)
+            step(evs[i])
+        torch.cuda.synchronize()
+    barrier(world)
+    stage_ms = {s: 0.0 for s in STAGES}
+    total_ms = 0.0
+    for e in evs:
+        total_ms += e[0].elapsed_time(e[5])
+        for j, s in enumerate(STAGES):
+            stage_ms[s] += e[j].elapsed_time(e[j + 1])
+    t_max = max_over_ranks(total_ms / 1e3, world)
+    value = world * flops * args.steps / t_max / 1e12
+    ms_step = 1e3 * t_max / args.steps
+    pk = peaks()
+    fp8_sus = 2.0 * pk["bf16_sus"]
+    l1_ms = stage_ms["expert_l1"] / args.steps
+    l1_flops = 4.0 * n_valid * w.H * w.I
+    l1_tf = l1_flops / (l1_ms / 1e3) / 1e12
+    traffic = measured_traffic() if w.name == "full" else None
+
+    # end to end through the public API: pinned host inputs -> GPU -> pinned host y
+    hx = d["x"].cpu().pin_memory()
+    hidx = d["topk_idx"].cpu().pin_memory()
+    htw = d["topk_w"].cpu().pin_memory()
+    hy = torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory()
+    gx, gidx, gtw = torch.empty_like(d["x"]), torch.empty_like(d["topk_idx"]), torch.empty_like(d["topk_w"])
+    e2e_ms = 0.0
+    for i in range(args.warmup + args.e2e_steps):
+        flush.fill_(3)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gx.copy_(hx, non_blocking=True)
+        gidx.copy_(hidx, non_blocking=True)
+        gtw.copy_(htw, non_blocking=True)
+        pp = moe.plan(gidx, gtw, w.E, w.H, w.I, workspace=ws)
+        moe.forward(gx, W1, W2, pp, y)
+        hy.copy_(y, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms += a.elapsed_time(b)
+    e2e_t = max_over_ranks(e2e_ms / 1e3, world)
+    e2e_val = world * flops * args.e2e_steps / e2e_t / 1e12
+    h2d = hx.numel() * 2 + hidx.numel() * 8 + htw.numel() * 4
+    d2h = hy.numel() * 2
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, d, args.cpu_tokens)
+    if rank != 0:
+        return
+    line = dict(
+        metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="e4m3 x e2m1 -> fp32 (MXFP8 x MXFP4, UE8M0/32)", data="synthetic",
+        config=dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}", T=w.T, H=w.H, I=w.I, E=w.E,
+                    k=w.k, valid_entries=n_valid, l2="flushed before every timed step (512 MB write)",
+                    parallelism=f"replicas x{world}"),
+        tokens_per_s=world * w.T * args.steps / t_max,
+        pct_fp8_peak=value / fp8_sus,
+        fp8_peak_tflops=dict(value=fp8_sus, note=f"2 x {pk['source']} sustained bf16 cuBLAS rate"),
+        stage_ms={s: v / args.steps for s, v in stage_ms.items()},
+        roofline=dict(kernel="expert_gemm_kernel<1> (L1)", bound="tensor", achieved=l1_tf, peak=fp8_sus,
+                      unit="TFLOP/s", frac=l1_tf / fp8_sus, traffic=traffic,
+                      algorithmic=f"4*N*H*I = {l1_flops:.4g} FLOP per launch (valid rows only)",
+                      peak_note=f"FP8 = 2 x {pk['source']} sustained bf16 ({pk['bf16_sus']} TF/s)"),
+        e2e=dict(value=e2e_val, unit="TFLOP/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                 ms_per_step=1e3 * e2e_t / args.e2e_steps),
+        gpu_launches=KERNELS_PER_STEP * args.steps,
+        clocks=clk.summary(),
+        cpu_baseline=cpu,
+    )
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

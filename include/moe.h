@@ -1,0 +1,182 @@
+/*
+ * moe.h -- C ABI of the single-GPU fused Mixture-of-Experts layer forward
+ * (GB300, sm_103a).
+ *
+ * What the layer computes (the DeepGEMM "Mega MoE" forward as analysed in the
+ * pages "DeepEP -> Mega MoE: the boundary evolution of communication and
+ * compute" and "Dispatch/Combine in the DeepGEMM Mega MoE kernel"), with every
+ * expert local to one GPU:
+ *
+ *   dispatch  per-expert counts of the top-k entries, exclusive prefix sums,
+ *             a deterministic slot per entry in an expert-major pool whose
+ *             expert segments are padded to MOE_BLOCK_M rows, then a gather of
+ *             token-major bf16 x into that pool with MXFP8 quantisation
+ *             (E4M3 codes, one UE8M0 scale per 32 hidden elements);
+ *   expert    L1 = pool x W1^T (FP8 x FP4 block-scaled, fp32 accumulate),
+ *             gate/up rounded to bf16, h = silu(gate) * up * topk_weight,
+ *             requantised to MXFP8 along I; L2 = h x W2^T rounded to bf16;
+ *   combine   y[t] = bf16( fp32 sum over ascending j of the valid entries'
+ *             L2 rows ); 0 for tokens with no valid entry.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except
+ *     where a comment says "host".  The library allocates no device memory;
+ *     every scratch buffer lives in the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).  All
+ *     work is enqueued on it; no call synchronises the host except
+ *     moe_plan_check().
+ *   - Every call returns a moe_status (0 = MOE_OK).  Nothing is thrown across
+ *     the ABI and no kernel traps: errors found on the device (bad expert id,
+ *     a bounded wait that expired) are recorded in the workspace and reported
+ *     by moe_plan_check().
+ *   - Shapes: x, y are [T, H] bf16 row-major; topk_idx [T, k] int64 with -1
+ *     meaning "not routed here"; topk_w [T, k] float32.  Requirements:
+ *     H % 128 == 0, I % 128 == 0, 1 <= k <= 32, 1 <= E <= 1024, T >= 0.
+ */
+#ifndef MOE_GB300_MOE_H_
+#define MOE_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape, plan mismatch */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape outside the requirements above, or not an sm_103 device */
+    MOE_ERR_WORKSPACE = 3,     /* workspace smaller than moe_plan_workspace_bytes() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    MOE_ERR_BAD_EXPERT_ID = 5, /* device saw topk_idx outside [-1, E); those entries were skipped */
+    MOE_ERR_TIMEOUT = 6,       /* a bounded device-side wait expired; outputs are invalid */
+    MOE_ERR_NO_KERNEL = 7      /* the library holds no code for this device */
+} moe_status;
+
+/* Rows of one MMA tile; every expert's pool segment is padded to it
+ * ("each expert's slots are aligned to BLOCK_M", Dispatch/Combine page,
+ * Appendix A.2). */
+#define MOE_BLOCK_M 128
+
+/* Plan: caller-owned opaque storage, filled by moe_plan().  It records the
+ * shapes and the workspace pointer; all device state lives in the
+ * workspace.  It may be copied by value. */
+typedef struct moe_plan_t {
+    uint64_t opaque[24];
+} moe_plan_t;
+
+/* One MXFP4 weight tensor [E, N, K].
+ *   q       e2m1 codes, two per byte, the even K index in the low nibble,
+ *           bit 3 of a nibble = sign; [E][N][K/2] bytes, 32-byte aligned.
+ *   sf_mma  UE8M0 scales (biased exponents, one per 32 along K) in the
+ *           tensor-core layout written by moe_prepare_weight_scales().
+ * W1 has N = 2I (gate rows 0..I-1, then up rows I..2I-1), K = H.
+ * W2 has N = H, K = I. */
+typedef struct moe_weights_t {
+    const void* q;
+    const void* sf_mma;
+    int32_t E, N, K;
+} moe_weights_t;
+
+/* Bytes of device workspace that moe_plan() needs for these shapes: routing
+ * tables, the expert-major MXFP8 pool, the requantised L1 output and the L2
+ * output.  Returns 0 if the shapes are unsupported.  Host-only, no CUDA. */
+size_t moe_plan_workspace_bytes(int T, int k, int E, int H, int I);
+
+/* Bytes of the tensor-core scale layout for an [E, N, K] weight.  0 if
+ * N % 128 or K % 128 is nonzero.  Host-only. */
+size_t moe_weight_scales_bytes(int E, int N, int K);
+
+/* One-time relayout of weight scales (not part of the per-batch path; the
+ * pages' "transformed_l1_weights" plays the same role).
+ *   sf      UE8M0 bytes [E][N][K/32] (device, row-major)
+ *   sf_mma  output, moe_weight_scales_bytes(E,N,K) bytes (device)
+ * Errors: MOE_ERR_INVALID_ARG (null pointers, small buffer),
+ * MOE_ERR_UNSUPPORTED (N or K not multiples of 128), MOE_ERR_CUDA. */
+int moe_prepare_weight_scales(const void* sf, int E, int N, int K, void* sf_mma,
+                              size_t sf_mma_bytes, void* stream);
+
+/* Dispatch plan (DeepEP -> Mega MoE page, dispatch.cuh snippet: expert count,
+ * prefix sum, slot assignment; Dispatch/Combine page section 3.1).
+ * Enqueues three kernels: per-chunk expert histograms (warp-aggregated
+ * shared-memory atomics), a prefix sum over chunks and experts (offsets,
+ * row-block-padded offsets, the tile table), and a stable slot per entry:
+ * slot = padded offset of its expert + number of earlier (smaller flat index
+ * t*k+j) entries of the same expert.  Entries with id -1 are skipped; ids
+ * outside [-1, E) are skipped and flagged (MOE_ERR_BAD_EXPERT_ID, via
+ * moe_plan_check).
+ *   plan       out (host): filled on success
+ *   topk_idx   [T, k] int64, device; read only by this call
+ *   topk_w     [T, k] float32, device; copied into the workspace
+ *   workspace  >= moe_plan_workspace_bytes(T,k,E,H,I) bytes, device,
+ *              256-byte aligned; owned by the caller, must stay alive and
+ *              untouched while the plan is used
+ * No host synchronisation.  T == 0 is a valid empty plan. */
+int moe_plan(moe_plan_t* plan, const int64_t* topk_idx, const float* topk_w, int T, int k, int E,
+             int H, int I, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dispatch gather (Dispatch/Combine page section 3.1, token pull into the
+ * expert pool; recipe (1,1,32) of the Normal-vs-Low-Latency page section 2):
+ * for each valid entry, pool row slot = MXFP8(x[t]).  x [T, H] bf16. */
+int moe_dispatch(const moe_plan_t* plan, const void* x, void* stream);
+
+/* Expert L1 (DeepEP -> Mega MoE page, sm100_fp8_fp4_mega_moe.cuh snippets:
+ * block-scaled FP8 x FP4 MMA, SwiGLU, amax, FP8 requant): for every pool row
+ * block, tcgen05 block-scaled MMA over H, then the epilogue
+ * h = silu(bf16(gate)) * bf16(up) * topk_weight, requantised to MXFP8.
+ * W1: E, N = 2I, K = H must match the plan. */
+int moe_expert_l1(const moe_plan_t* plan, const moe_weights_t* W1, void* stream);
+
+/* Expert L2: pool rows of h x W2^T, fp32 accumulate, rounded to bf16 rows in
+ * pool order (Dispatch/Combine page section 5.1, the unweighted bf16
+ * combine buffer).  W2: E, N = H, K = I must match the plan. */
+int moe_expert_l2(const moe_plan_t* plan, const moe_weights_t* W2, void* stream);
+
+/* Combine (DeepEP -> Mega MoE page, combine_utils.cuh snippet; Dispatch/
+ * Combine page section 5.1): y[t] = bf16(fp32 sum over ascending j of the
+ * valid entries' L2 rows), y[t] = 0 if token t has no valid entry.
+ * y [T, H] bf16. */
+int moe_combine(const moe_plan_t* plan, void* y, void* stream);
+
+/* The whole layer after moe_plan(): moe_dispatch + moe_expert_l1 +
+ * moe_expert_l2 + moe_combine, in stream order. */
+int moe_forward(const void* x, const moe_weights_t* W1, const moe_weights_t* W2,
+                const moe_plan_t* plan, void* y, void* stream);
+
+/* Synchronises `stream`, then returns the first device-side error recorded
+ * in the plan's workspace (MOE_ERR_BAD_EXPERT_ID, MOE_ERR_TIMEOUT) or
+ * MOE_OK.  The record is cleared by the next moe_plan() on that workspace. */
+int moe_plan_check(const moe_plan_t* plan, void* stream);
+
+/* Where an internal array of the plan lives inside the workspace, for tests
+ * and tools: byte offset and size.  `what` is one of MOE_EXPORT_*. */
+enum {
+    MOE_EXPORT_COUNT = 0,        /* int32 [E] */
+    MOE_EXPORT_OFFSETS = 1,      /* int32 [E+1] exclusive scan of counts */
+    MOE_EXPORT_POFFSETS = 2,     /* int32 [E+1] exclusive scan of counts padded to MOE_BLOCK_M */
+    MOE_EXPORT_SLOT_OF = 3,      /* int32 [T*k] pool row of entry (t,j), -1 if skipped */
+    MOE_EXPORT_ROW_TOKEN = 4,    /* int32 [P_cap] token of a pool row, -1 on padding */
+    MOE_EXPORT_ROW_TOPK = 5,     /* int32 [P_cap] j of a pool row, -1 on padding */
+    MOE_EXPORT_ROW_WEIGHT = 6,   /* float [P_cap] topk weight of a pool row */
+    MOE_EXPORT_BLOCK_EXPERT = 7, /* int32 [P_cap/128] expert of each pool row block */
+    MOE_EXPORT_NUM_BLOCKS = 8,   /* int32 [1] number of pool row blocks in use */
+    MOE_EXPORT_POOL_Q = 9,       /* uint8 [P_cap, H] E4M3 pool */
+    MOE_EXPORT_POOL_SF = 10,     /* uint8 [P_cap/128][H/128][512] UE8M0, tensor-core layout */
+    MOE_EXPORT_H_Q = 11,         /* uint8 [P_cap, I] E4M3 requantised L1 output */
+    MOE_EXPORT_H_SF = 12,        /* uint8 [P_cap/128][I/128][512] UE8M0, tensor-core layout */
+    MOE_EXPORT_L2_OUT = 13,      /* bf16 [P_cap, H] L2 output rows in pool order */
+    MOE_EXPORT_ERROR = 14,       /* int32 [2] device error record: bits, then where a wait expired */
+    MOE_EXPORT_POOL_ROWS = 15    /* (size only) P_cap, the pool row capacity, in the size field */
+};
+int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* bytes);
+
+/* Static text for a status code. */
+const char* moe_error_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H_ */

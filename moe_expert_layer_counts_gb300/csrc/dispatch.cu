@@ -1,0 +1,90 @@
+// dispatch.cu -- gather of token-major bf16 activations into the expert-major
+// pool with MXFP8 quantisation (page "Dispatch/Combine in the DeepGEMM Mega
+// MoE kernel", section 3.1: the token pull into l1_token_buffer; Appendix A.1
+// for the FP8 token buffer with its scale buffer; recipe (1,1,32) of the
+// "Normal vs Low-Latency" page, section 2).
+//
+// The pages quantise upstream and move FP8 rows with 1-D TMA copies.  Here
+// the quantisation is fused into the gather: each token row is read once,
+// quantised once (E4M3 codes, one UE8M0 byte per 32 elements), and written to
+// each of its k pool rows.  One warp handles a 1024-element segment of one
+// token; a lane owns 8 consecutive elements, four lanes one 32-block.
+// Scales are written directly in the tensor-core layout the GEMM consumes:
+// chunk (row/128, col/128) of 512 bytes, byte 16*(row%32) + 4*((row%128)/32)
+// + (col/32)%4.
+#include <cuda_runtime.h>
+
+#include "formats.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kSeg = 1024;  // elements per warp work item
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
+                                                                   const int* __restrict__ slot_of,
+                                                                   uint8_t* __restrict__ pool_q,
+                                                                   uint8_t* __restrict__ pool_sf) {
+    const int lane = threadIdx.x & 31;
+    const int nseg = (H + kSeg - 1) / kSeg;
+    const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    const int t = static_cast<int>(item / nseg);
+    if (t >= T) return;
+    const int seg = static_cast<int>(item % nseg);
+    const int my_slot = lane < k ? __ldg(slot_of + static_cast<size_t>(t) * k + lane) : -1;
+    const int s_begin = seg * kSeg, s_end = min(s_begin + kSeg, H);
+    const int sf_cols = H / 128;
+    for (int s0 = s_begin; s0 < s_end; s0 += 256) {
+        const int col = s0 + lane * 8;
+        const bool active = col < s_end;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (active) raw = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + col));
+        float f[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
+                      bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t sbyte = ue8m0_scale_e4m3(amax);
+        const float inv = inv_scale_from_byte(sbyte);
+        uint2 codes;
+        codes.x = e4m3x2(f[0] * inv, f[1] * inv) | (e4m3x2(f[2] * inv, f[3] * inv) << 16);
+        codes.y = e4m3x2(f[4] * inv, f[5] * inv) | (e4m3x2(f[6] * inv, f[7] * inv) << 16);
+        // scale word of the 128-column group owned by lanes 0..15 / 16..31
+        const int g = lane & 16;
+        const uint32_t sw = __shfl_sync(0xffffffffu, sbyte, g) | (__shfl_sync(0xffffffffu, sbyte, g + 4) << 8) |
+                            (__shfl_sync(0xffffffffu, sbyte, g + 8) << 16) |
+                            (__shfl_sync(0xffffffffu, sbyte, g + 12) << 24);
+        for (int j = 0; j < k; ++j) {
+            const int r = __shfl_sync(0xffffffffu, my_slot, j);
+            if (r < 0) continue;
+            if (active) {
+                *reinterpret_cast<uint2*>(pool_q + static_cast<size_t>(r) * H + col) = codes;
+                if ((lane & 15) == 0) {
+                    const size_t chunk = static_cast<size_t>(r / kBlockM) * sf_cols + col / 128;
+                    const int m = r % kBlockM;
+                    *reinterpret_cast<uint32_t*>(pool_sf + chunk * kSfChunkBytes + 16 * (m % 32) + 4 * (m / 32)) =
+                        sw;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, cudaStream_t s) {
+    if (L.T == 0) return cudaSuccess;
+    const int nseg = (L.H + kSeg - 1) / kSeg;
+    const int64_t items = static_cast<int64_t>(L.T) * nseg;
+    const int64_t blocks = (items + kThreads / 32 - 1) / (kThreads / 32);
+    dispatch_quant_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
+        static_cast<const uint16_t*>(x), L.T, L.H, L.k, reinterpret_cast<const int*>(ws + L.slot_of),
+        ws + L.pool_q, ws + L.pool_sf);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,446 @@
+// expert_gemm.cu -- persistent grouped GEMM over the expert-major pool on the
+// 5th-generation tensor cores: A = pool rows (E4M3), B = expert weights
+// (E2M1), UE8M0 scales per 32 along K, fp32 accumulation in tensor memory
+// (page "DeepEP -> Mega MoE", sm100_fp8_fp4_mega_moe.cuh snippets: the
+// block-scaled MXF8F6F4 MMA, the TMA-A / TMA-B / MMA / epilogue warp roles,
+// the SwiGLU + amax + FP8 requant epilogue; "Normal vs Low-Latency" page
+// sections 3 and 5: one persistent CTA per SM, pipeline depth set by shared
+// memory).
+//
+// Layer 1: a work item is (pool row block b, intermediate tile j of 128).  The
+//   MMA has N = 256: weight rows gate [j*128, +128) and up [I + j*128, +128)
+//   are loaded as two TMA boxes into one B tile, so SwiGLU is tile-local.
+//   Epilogue per pool row: g = bf16(acc_gate), u = bf16(acc_up),
+//   h = (g / (1 + exp(-g))) * u * topk_weight in fp32, requantised per 32 to
+//   E4M3 + UE8M0 (scales written in the tensor-core layout L2 reads).
+// Layer 2: a work item is (pool row block b, output tile j of 256 columns);
+//   epilogue rounds the fp32 accumulators to bf16 rows in pool order.
+//
+// Warp roles (320 threads, one CTA per SM, persistent over work items):
+//   warp 0   TMA producer: A box, two B boxes, three scale chunks per stage
+//   warp 1   tensor-memory owner and MMA issuer (one elected thread)
+//   warps 2-9 epilogue; warp w reads tensor-memory lanes 32*(w%4)..+31 and
+//            one half of the accumulator columns ((w-2)/4), so two warps
+//            share each lane quadrant
+// Every wait is bounded (a global-timer deadline); on expiry the CTA records
+// an error in the workspace, waits for its own copies in flight, releases
+// tensor memory and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "formats.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBN = 256;                       // MMA N: two 128-row weight boxes
+constexpr int kABytes = kBlockM * kBlockK;     // 16 KB of E4M3
+constexpr int kBBoxBytes = 128 * kBlockK;      // 16 KB in smem: E2M1 unpacked to one byte per element
+constexpr int kBBoxTxBytes = 128 * kBlockK / 2; // the box's transaction count is its packed size
+constexpr int kBBytes = 2 * kBBoxBytes;
+constexpr int kSfaOff = kABytes + kBBytes;     // 512 B
+constexpr int kSfbOff = kSfaOff + kSfChunkBytes;  // 2 x 512 B
+constexpr int kStageTxBytes = kABytes + 2 * kBBoxTxBytes + 3 * kSfChunkBytes;
+constexpr int kStageStride = 51200;            // multiple of 1024 (swizzle atom alignment)
+static_assert(kSfbOff + 2 * kSfChunkBytes <= kStageStride, "stage overflow");
+constexpr int kBarrierBytes = 256;
+constexpr int kSmemBytes = kStages * kStageStride + kBarrierBytes + 1024;
+constexpr int kTmemCols = 512;
+constexpr int kSfTmemCol = 256;                // scale slots: 16 columns per stage
+constexpr int kThreads = 320;                  // 10 warps: TMA, MMA, 8 epilogue
+constexpr int kEpiWarps = 8;
+constexpr uint64_t kWaitNs = 1000000000ull;    // 1 s per wait
+
+struct GemmParams {
+    const int* n_blocks;
+    const int* block_expert;
+    const int* row_token;
+    const float* row_weight;
+    const uint8_t* sfa;     // activation scales, chunks [P_cap/128][K/128]
+    const uint8_t* sfb;     // weight scales, chunks [E][N/128][K/128]
+    uint8_t* out_q;         // layer 1: E4M3 h [P_cap, I]
+    uint8_t* out_sf;        // layer 1: scales of h, chunks [P_cap/128][I/128]
+    uint16_t* out_bf16;     // layer 2: bf16 rows [P_cap, H]
+    int K;                  // reduction length
+    int N;                  // weight rows per expert
+    int n_tiles;            // work items per pool row block
+    int I;                  // layer 1: intermediate size
+    int H;                  // layer 2: output columns
+    int* err;
+};
+
+struct Shared {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tmem_full;
+    uint64_t tmem_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// On expiry the first CTA to give up records where: err[1] = 1 + where, with
+// where = stage (producer waiting on empty), 16 (MMA on tmem_empty),
+// 32 + stage (MMA on full), 48 (epilogue on tmem_full).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, Shared* sh, int* err, int where) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::mbar_wait(bar, parity, ptx::globaltimer() + kWaitNs)) return true;
+    atomicOr(err, kDevErrTimeout);
+    atomicCAS(err + 1, 0, 1 + where);
+    *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+    return false;
+}
+__device__ __forceinline__ bool aborted(Shared* sh) { return *reinterpret_cast<volatile int*>(&sh->abort) != 0; }
+
+// SwiGLU of one value by the exact definition, (float)(g / (1 + exp(-g))) in
+// double; kept out of line so the rare callers stay small.
+__device__ __noinline__ float silu_exact(float g) {
+    return static_cast<float>(static_cast<double>(g) / (1.0 + exp(-static_cast<double>(g))));
+}
+
+// SwiGLU * topk weight and MXFP8 requantisation of 32 intermediate columns
+// of one pool row ("DeepEP -> Mega MoE" page, SwiGLU / amax / FP8 cast
+// snippets).  gu holds (bf16 gate, bf16 up) pairs.  The fast path uses
+// __expf and an approximate divide (error well below kDecisionUlps for
+// |gate| <= 16).  Wherever that could change an integer decision under the
+// exact formula, the exact value is used instead: an element within
+// kDecisionUlps of an E4M3 code midpoint (or with |gate| > 16) is recomputed
+// alone; if the block maximum lies that close to the UE8M0 scale boundary,
+// the whole block is recomputed.  So every code and scale byte is the one the
+// exact definition gives.  Writes 32 E4M3 codes to dst (16-byte aligned) and
+// returns the scale byte.
+constexpr uint32_t kDecisionUlps = 64;
+
+__device__ __forceinline__ uint32_t requant_block(const uint32_t* gu, float wgt, uint8_t* dst) {
+    float h[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float g = bf16_lo(gu[i]), u = bf16_hi(gu[i]);
+        const float silu = fabsf(g) > 16.0f ? silu_exact(g) : __fdividef(g, 1.0f + __expf(-g));
+        h[i] = (silu * u) * wgt;
+        amax = fmaxf(amax, fabsf(h[i]));
+    }
+    if (near_e4m3_scale_boundary(amax, kDecisionUlps)) {
+        amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            h[i] = (silu_exact(bf16_lo(gu[i])) * bf16_hi(gu[i])) * wgt;
+            amax = fmaxf(amax, fabsf(h[i]));
+        }
+    }
+    const uint32_t sbyte = ue8m0_scale_e4m3(amax);
+    const float inv = inv_scale_from_byte(sbyte);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (near_e4m3_midpoint(h[i] * inv, kDecisionUlps))
+            h[i] = (silu_exact(bf16_lo(gu[i])) * bf16_hi(gu[i])) * wgt;
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        q[i] = e4m3x2(h[4 * i] * inv, h[4 * i + 1] * inv) | (e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv) << 16);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+    d[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    d[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    return sbyte;
+}
+
+template <int kLayer>
+__global__ void __launch_bounds__(kThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                       const GemmParams p) {
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared* sh = reinterpret_cast<Shared*>(smem + kStages * kStageStride);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int n_work = *p.n_blocks * p.n_tiles;
+    if (static_cast<int>(blockIdx.x) >= n_work) return;  // uniform for the CTA
+    const int kb_count = p.K / kBlockK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sh->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh->empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&sh->tmem_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&sh->tmem_empty), kEpiWarps);
+        ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
+        sh->abort = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&tmap_a);
+        ptx::prefetch_tensormap(&tmap_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(&sh->tmem_base), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&sh->tmem_base);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        bool ok = true;
+        const int nb_per_expert = p.N / 128;
+        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+            const int b = w / p.n_tiles, j = w % p.n_tiles;
+            const int e = __ldg(p.block_expert + b);
+            int nb0, nb1;
+            if (kLayer == 1) {
+                nb0 = j;                       // gate rows j*128..
+                nb1 = p.I / 128 + j;           // up rows I + j*128..
+            } else {
+                nb0 = 2 * j;
+                nb1 = min(2 * j + 1, nb_per_expert - 1);  // tail tile of an odd H/128: re-read, ignored
+            }
+            const int row_b0 = e * p.N + nb0 * 128;
+            const int row_b1 = e * p.N + (kLayer == 1 ? nb1 * 128 : (2 * j + 1) * 128);
+            const uint8_t* sfb0 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb0) * kb_count * kSfChunkBytes;
+            const uint8_t* sfb1 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb1) * kb_count * kSfChunkBytes;
+            const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
+            for (int kb = 0; kb < kb_count; ++kb) {
+                if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + stage * kStageStride;
+                const uint32_t full = ptx::smem_addr(&sh->full[stage]);
+                ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
+                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a, kb * kBlockK, b * kBlockM, full);
+                ptx::tma_load_2d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, row_b0, full);
+                ptx::tma_load_2d(ptx::smem_addr(st + kABytes + kBBoxBytes), &tmap_b, kb * kBlockK, row_b1, full);
+                ptx::bulk_load(ptx::smem_addr(st + kSfaOff), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
+                ptx::bulk_load(ptx::smem_addr(st + kSfbOff), sfb0 + kb * kSfChunkBytes, kSfChunkBytes, full);
+                ptx::bulk_load(ptx::smem_addr(st + kSfbOff + kSfChunkBytes), sfb1 + kb * kSfChunkBytes,
+                               kSfChunkBytes, full);
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            // let this CTA's copies in flight land before the CTA may exit
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    ptx::mbar_wait(ptx::smem_addr(&sh->full[s]), (issued_parity >> s) & 1u,
+                                   ptx::globaltimer() + kWaitNs);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = ptx::idesc_e4m3_e2m1(kBlockM, kBN);
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+            if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->tmem_empty), acc_phase ^ 1, sh, p.err, 16)) break;
+            ptx::tc_fence_after();
+            for (int kb = 0; kb < kb_count; ++kb) {
+                if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->full[stage]), phase, sh, p.err, 32 + stage)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t st = ptx::smem_addr(smem + stage * kStageStride);
+                const uint32_t tsf = tmem + kSfTmemCol + 16 * stage;
+                ptx::tc_cp_32x128b_warpx4(tsf + 0, ptx::desc_sf_32x16(st + kSfaOff));
+                ptx::tc_cp_32x128b_warpx4(tsf + 4, ptx::desc_sf_32x16(st + kSfbOff));
+                ptx::tc_cp_32x128b_warpx4(tsf + 8, ptx::desc_sf_32x16(st + kSfbOff + kSfChunkBytes));
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / 32; ++kk) {
+                    const uint64_t a_desc = ptx::desc_kmajor_sw128(st + kk * 32);
+                    const uint64_t b_desc = ptx::desc_kmajor_sw128(st + kABytes + kk * 32);
+                    ptx::mma_mxf8f6f4(tmem, a_desc, b_desc, ptx::idesc_with_sf_id(idesc, kk), tsf + 0, tsf + 4,
+                                      (kb | kk) != 0);
+                }
+                ptx::tc_commit(ptx::smem_addr(&sh->empty[stage]));
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            ptx::tc_commit(ptx::smem_addr(&sh->tmem_full));
+            acc_phase ^= 1;
+        }
+        // all tensor-core work of this CTA done before tensor memory is freed
+        ptx::tc_commit(ptx::smem_addr(&sh->drain));
+        ptx::mbar_wait(ptx::smem_addr(&sh->drain), 0, ptx::globaltimer() + kWaitNs);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        const int half = (warp - 2) / 4;                // which half of the accumulator columns
+        const int m = quad * 32 + lane;                 // row of the tile = tensor-memory lane
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        uint32_t acc_phase = 0;
+        for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
+            const int b = w / p.n_tiles, j = w % p.n_tiles;
+            const int r = b * kBlockM + m;
+            const int tok = __ldg(p.row_token + r);
+            const float wgt = __ldg(p.row_weight + r);
+            // tcgen05.ld is warp-collective: the whole warp goes on or stops together
+            const bool go = !aborted(sh) && wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p.err, 48);
+            if (!__all_sync(0xffffffffu, go)) break;
+            ptx::tc_fence_after();
+            // Drain this warp's half of the accumulator row into registers as
+            // packed bf16 pairs and release tensor memory at once, so the next
+            // tile's MMAs overlap the rest of the epilogue.  (Layer 1 rounds
+            // gate/up to bf16 here anyway; layer 2 rounds its output to bf16.)
+            uint32_t pk[64];
+            if (kLayer == 1) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t g[16], u[16];
+                    ptx::tmem_ld_32x32b_x16(t_row + 64 * half + 16 * c, g);
+                    ptx::tmem_ld_32x32b_x16(t_row + 128 + 64 * half + 16 * c, u);
+                    ptx::tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[16 * c + i] = bf16x2_rn(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(t_row + 128 * half + 32 * c, v);
+                    ptx::tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        pk[16 * c + i] = bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
+            if (tok >= 0) {
+                if (kLayer == 1) {
+                    // intermediate columns j*128 + 64*half + [0, 64): two 32-blocks
+                    uint8_t* dst = p.out_q + static_cast<size_t>(r) * p.I + j * 128 + 64 * half;
+                    const uint32_t s0 = requant_block(pk, wgt, dst);
+                    const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32);
+                    const size_t chunk = static_cast<size_t>(b) * (p.I / 128) + j;
+                    *reinterpret_cast<uint16_t*>(p.out_sf + chunk * kSfChunkBytes + 16 * lane + 4 * quad + 2 * half) =
+                        static_cast<uint16_t>(s0 | (s1 << 8));
+                } else {
+                    const int col0 = j * kBN + 128 * half;
+                    const int ncol = p.H - col0;
+                    uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + static_cast<size_t>(r) * p.H + col0);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (8 * i < ncol) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            acc_phase ^= 1;
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+#else
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kDevErrTimeout);
+#endif
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the
+// library does not link libcuda directly.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D K-major tile map: rows x K, box 128 rows x 128 K elements, 128-byte swizzle.
+bool make_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t k_elems, uint64_t rows,
+              uint64_t row_bytes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {k_elems, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,
+                               cudaStream_t s) {
+    if (L.T == 0) return cudaSuccess;
+    GemmParams p{};
+    p.n_blocks = reinterpret_cast<const int*>(ws + L.n_blocks);
+    p.block_expert = reinterpret_cast<const int*>(ws + L.block_expert);
+    p.row_token = reinterpret_cast<const int*>(ws + L.row_token);
+    p.row_weight = reinterpret_cast<const float*>(ws + L.row_weight);
+    p.sfb = static_cast<const uint8_t*>(g.w_sf);
+    p.K = g.K;
+    p.N = g.N;
+    p.I = L.I;
+    p.H = L.H;
+    p.err = reinterpret_cast<int*>(ws + L.err);
+    CUtensorMap map_a, map_b;
+    const void* a_base;
+    if (layer == 1) {
+        a_base = ws + L.pool_q;
+        p.sfa = ws + L.pool_sf;
+        p.out_q = ws + L.h_q;
+        p.out_sf = ws + L.h_sf;
+        p.n_tiles = L.I / 128;
+    } else {
+        a_base = ws + L.h_q;
+        p.sfa = ws + L.h_sf;
+        p.out_bf16 = reinterpret_cast<uint16_t*>(ws + L.l2_out);
+        p.n_tiles = (L.H + kBN - 1) / kBN;
+    }
+    if (!make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K) ||
+        !make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K, static_cast<uint64_t>(g.E) * g.N,
+                  g.K / 2))
+        return cudaErrorInvalidValue;
+    static int attr_done[2][64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaError_t st;
+    if (layer == 1) {
+        if (dev < 64 && !attr_done[0][dev]) {
+            st = cudaFuncSetAttribute(expert_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (st != cudaSuccess) return st;
+            attr_done[0][dev] = 1;
+        }
+        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_b, p);
+    } else {
+        if (dev < 64 && !attr_done[1][dev]) {
+            st = cudaFuncSetAttribute(expert_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (st != cudaSuccess) return st;
+            attr_done[1][dev] = 1;
+        }
+        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_b, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

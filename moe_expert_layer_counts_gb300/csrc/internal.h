@@ -1,0 +1,64 @@
+// internal.h -- workspace layout and the launchers shared by the C-ABI
+// translation unit and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kBlockM = MOE_BLOCK_M;   // pool rows per MMA tile
+constexpr int kBlockK = 128;           // K per pipeline stage (one scale chunk)
+constexpr int kSfVec = 32;             // elements per UE8M0 scale
+constexpr int kSfChunkBytes = 512;     // 128 rows x 4 scales, tensor-core layout
+constexpr int kRouteChunk = 2048;      // top-k entries per routing CTA
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopk = 32;
+
+// Device-side error bits recorded in the workspace (word 0); word 1 records
+// where a bounded wait expired.
+constexpr int kDevErrBadExpert = 1;
+constexpr int kDevErrTimeout = 2;
+
+// Byte offsets of every array inside the caller's workspace.
+struct Layout {
+    int T, k, E, H, I;
+    int chunks;        // routing chunks (CTAs of the count / slot kernels)
+    int64_t p_cap;     // pool row capacity (multiple of kBlockM)
+    size_t err, n_blocks, count, off, poff, hist, chunk_base, block_expert;
+    size_t slot_of, row_token, row_topk, row_weight;
+    size_t pool_q, pool_sf, h_q, h_sf, l2_out;
+    size_t total;
+};
+
+bool make_layout(int T, int k, int E, int H, int I, Layout* L);
+
+// Plan storage behind moe_plan_t.
+struct PlanState {
+    uint64_t magic;
+    uint8_t* ws;
+    size_t ws_bytes;
+    int32_t T, k, E, H, I, device;
+};
+static_assert(sizeof(PlanState) <= sizeof(moe_plan_t), "plan storage too small");
+constexpr uint64_t kPlanMagic = 0x4D6F45506C616E31ull;  // "MoEPlan1"
+
+// Launchers (enqueue only; return cudaError_t of the launch).
+cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, const float* topk_w,
+                         cudaStream_t s);
+cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, cudaStream_t s);
+cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s);
+cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, uint8_t* out, cudaStream_t s);
+
+struct GemmLaunch {
+    const void* w_q;      // packed e2m1 weights [E, N, K/2]
+    const void* w_sf;     // tensor-core scale layout
+    int E, N, K;
+};
+// layer 1: pool x W1 -> requantised h; layer 2: h x W2 -> bf16 rows.
+cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,
+                               cudaStream_t s);
+
+}  // namespace moe

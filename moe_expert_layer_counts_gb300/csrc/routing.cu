@@ -1,0 +1,218 @@
+// routing.cu -- dispatch plan: per-expert counts, prefix sums and a stable
+// slot per top-k entry (page "DeepEP -> Mega MoE", dispatch.cuh snippet:
+// expert counting with block-scope atomics, do_psum prefix sum, slot
+// assignment; page "Dispatch/Combine in the DeepGEMM Mega MoE kernel",
+// section 3.1 and Appendix A.2 for the expert-major pool padded to the row
+// block).
+//
+// The pages assign slots with a global atomicAdd, so the order of tokens
+// inside an expert is not reproducible.  Here the slot of entry i = t*k+j is
+// its expert's padded offset plus the number of entries of the same expert
+// with a smaller flat index -- a stable counting sort -- computed with three
+// kernels and no atomics on the result:
+//   route_count  one CTA per chunk of kRouteChunk entries: shared-memory
+//                histogram, warp-aggregated (one atomic per distinct expert
+//                per warp, via __match_any_sync)
+//   route_scan   one CTA: per-expert prefix over chunks, exclusive scans of
+//                counts and of counts padded to MOE_BLOCK_M, the row-block ->
+//                expert table and the number of row blocks
+//   route_slot   one CTA per chunk: ranks inside the chunk in flat order
+//                (rank in warp from the match mask, plus same-expert counts of
+//                lower warps), inverse maps of every pool row, padding rows
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kCountThreads = 256;
+constexpr int kSlotThreads = 256;
+constexpr int kSlotWarps = kSlotThreads / 32;
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Expert id of entry i, or -1 for skipped / out-of-range entries.
+__device__ __forceinline__ int entry_expert(const int64_t* idx, int64_t i, int64_t end, int E, bool* bad) {
+    if (i >= end) return -1;
+    const int64_t v = __ldg(idx + i);
+    if (v < -1 || v >= E) {
+        *bad = true;
+        return -1;
+    }
+    return static_cast<int>(v);
+}
+
+__global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int64_t* __restrict__ topk_idx,
+                                                                     int64_t n_entries, int E,
+                                                                     int* __restrict__ hist, int* __restrict__ err) {
+    extern __shared__ int s_hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+    const int64_t end = min(base + kRouteChunk, n_entries);
+    bool bad = false;
+    for (int64_t i0 = base; i0 < end; i0 += blockDim.x) {
+        const int e = entry_expert(topk_idx, i0 + threadIdx.x, end, E, &bad);
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(same) - 1) atomicAdd(&s_hist[e], __popc(same));
+    }
+    if (bad) atomicOr(err, kDevErrBadExpert);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
+}
+
+// Block-wide inclusive scan of one int per thread (blockDim.x == 1024).
+__device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += o;
+    }
+    if (lane == 31) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_warp[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += o;
+        }
+        s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int r = v + (warp > 0 ? s_warp[warp - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __restrict__ hist, int chunks, int E,
+                                                                   int* __restrict__ count, int* __restrict__ off,
+                                                                   int* __restrict__ poff,
+                                                                   int* __restrict__ chunk_base,
+                                                                   int* __restrict__ block_expert,
+                                                                   int* __restrict__ n_blocks) {
+    __shared__ int s_warp[32];
+    const int e = threadIdx.x;
+    int c_e = 0;
+    if (e < E) {
+#pragma unroll 8
+        for (int c = 0; c < chunks; ++c) {
+            const int v = hist[static_cast<size_t>(c) * E + e];
+            chunk_base[static_cast<size_t>(c) * E + e] = c_e;
+            c_e += v;
+        }
+        count[e] = c_e;
+    }
+    const int padded = (c_e + kBlockM - 1) / kBlockM * kBlockM;
+    const int inc_c = block_inclusive_scan(c_e, s_warp);
+    const int inc_p = block_inclusive_scan(padded, s_warp);
+    if (e < E) {
+        off[e] = inc_c - c_e;
+        poff[e] = inc_p - padded;
+        if (e == E - 1) {
+            off[E] = inc_c;
+            poff[E] = inc_p;
+            *n_blocks = inc_p / kBlockM;
+        }
+        const int b0 = (inc_p - padded) / kBlockM;
+        for (int b = 0; b < padded / kBlockM; ++b) block_expert[b0 + b] = e;
+    }
+}
+
+__global__ void __launch_bounds__(kSlotThreads) route_slot_kernel(
+    const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
+    const int* __restrict__ count, const int* __restrict__ poff, const int* __restrict__ chunk_base,
+    int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
+    float* __restrict__ row_weight) {
+    extern __shared__ int s_mem[];
+    int* s_next = s_mem;        // [E] next free slot of each expert for this chunk
+    int* s_wcnt = s_mem + E;    // [kSlotWarps][E] same-expert counts per warp, this round
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_next[e] = poff[e] + chunk_base[static_cast<size_t>(blockIdx.x) * E + e];
+        for (int w = 0; w < kSlotWarps; ++w) s_wcnt[w * E + e] = 0;
+    }
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+    const int64_t end = min(base + kRouteChunk, n_entries);
+    bool bad = false;
+    for (int64_t i0 = base; i0 < end; i0 += blockDim.x) {
+        const int64_t i = i0 + threadIdx.x;
+        const int e = entry_expert(topk_idx, i, end, E, &bad);
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const bool leader = lane == __ffs(same) - 1;
+        if (e >= 0 && leader) s_wcnt[warp * E + e] = __popc(same);
+        __syncthreads();
+        int slot = -1;
+        if (e >= 0) {
+            int before = __popc(same & lanemask_lt());
+            for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
+            slot = s_next[e] + before;
+        }
+        __syncthreads();
+        if (e >= 0 && leader) {
+            atomicAdd(&s_next[e], __popc(same));
+            s_wcnt[warp * E + e] = 0;
+        }
+        __syncthreads();
+        if (i < end) {
+            slot_of[i] = slot;
+            if (slot >= 0) {
+                row_token[slot] = static_cast<int>(i / k);
+                row_topk[slot] = static_cast<int>(i % k);
+                row_weight[slot] = __ldg(topk_w + i);
+            }
+        }
+    }
+    // padding rows of this CTA's share of experts
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        const int p0 = poff[e] + count[e], p1 = poff[e + 1];
+        for (int r = p0 + threadIdx.x; r < p1; r += blockDim.x) {
+            row_token[r] = -1;
+            row_topk[r] = -1;
+            row_weight[r] = 0.0f;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, const float* topk_w,
+                         cudaStream_t s) {
+    const int64_t n = static_cast<int64_t>(L.T) * L.k;
+    int* err = reinterpret_cast<int*>(ws + L.err);
+    int* hist = reinterpret_cast<int*>(ws + L.hist);
+    int* count = reinterpret_cast<int*>(ws + L.count);
+    int* off = reinterpret_cast<int*>(ws + L.off);
+    int* poff = reinterpret_cast<int*>(ws + L.poff);
+    int* chunk_base = reinterpret_cast<int*>(ws + L.chunk_base);
+    cudaError_t st = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
+    if (st != cudaSuccess) return st;
+    if (L.chunks > 0) {
+        route_count_kernel<<<L.chunks, kCountThreads, L.E * sizeof(int), s>>>(topk_idx, n, L.E, hist, err);
+        if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    }
+    route_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, L.chunks, L.E, count, off, poff, chunk_base,
+                                                 reinterpret_cast<int*>(ws + L.block_expert),
+                                                 reinterpret_cast<int*>(ws + L.n_blocks));
+    if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    if (L.chunks > 0) {
+        const size_t smem = static_cast<size_t>(L.E) * (1 + kSlotWarps) * sizeof(int);
+        route_slot_kernel<<<L.chunks, kSlotThreads, smem, s>>>(
+            topk_idx, topk_w, n, L.k, L.E, count, poff, chunk_base, reinterpret_cast<int*>(ws + L.slot_of),
+            reinterpret_cast<int*>(ws + L.row_token), reinterpret_cast<int*>(ws + L.row_topk),
+            reinterpret_cast<float*>(ws + L.row_weight));
+        if ((st = cudaGetLastError()) != cudaSuccess) return st;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

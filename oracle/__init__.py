@@ -74,7 +74,7 @@ def lib():
             L.or_quant_x.restype = None
             L.or_quant_x.argtypes = [P, i32, i32, P, P, i32]
             L.or_forward.restype = i32
-            L.or_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, i64, i32]
+            L.or_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P, i64, i32]
             L.or_combine.restype = None
             L.or_combine.argtypes = [P, P, i32, i32, i32, P]
             L.or_l2_row.restype = None
@@ -191,7 +191,8 @@ def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
     """Oracle forward.  x: uint16 bf16 bits [T,H]; w1q uint8 [E,2I,H/2]; w1sf uint8
     [E,2I,H/32]; w2q uint8 [E,H,I/2]; w2sf uint8 [E,H,I/32].
     tokens: optional int array of tokens to compute (y rows in that order).
-    want_pool: also return per-pool-row hq [p_cap,I], hsf [p_cap,I/32], o [p_cap,H].
+    want_pool: also return per-pool-row hq [p_cap,I], hsf [p_cap,I/32], o [p_cap,H] and the
+    pre-requantisation h [p_cap,I] (float32).
     Returns dict(y=uint16 bf16 bits, status, and pool arrays if asked)."""
     x = _c(x_bf16_bits, np.uint16)
     T, H = x.shape
@@ -210,18 +211,19 @@ def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
         toks = _c(tokens, np.int32)
         toks_p, ntok = _p(toks), toks.size
     y = np.zeros((ntok, H), np.uint16)
-    hq = hsf = o = None
+    hq = hsf = o = hf = None
     if want_pool and tokens is None:
         hq = np.zeros((p_cap, I), np.uint8)
         hsf = np.zeros((p_cap, I // SF_VEC), np.uint8)
         o = np.zeros((p_cap, H), np.uint16)
+        hf = np.zeros((p_cap, I), np.float32)
     st = lib().or_forward(_p(x), _p(idx), _p(w), T, k, E, H, I, _p(w1q), _p(w1sf), _p(w2q), _p(w2sf),
                           toks_p, ntok, _p(y),
                           _p(hq) if hq is not None else None, _p(hsf) if hsf is not None else None,
-                          _p(o) if o is not None else None, p_cap, nthreads)
+                          _p(o) if o is not None else None, _p(hf) if hf is not None else None, p_cap, nthreads)
     res.update(y=y, status=st)
     if hq is not None:
-        res.update(hq=hq, hsf=hsf, o=o)
+        res.update(hq=hq, hsf=hsf, o=o, h=hf)
     return res
 
 

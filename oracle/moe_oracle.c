@@ -288,14 +288,16 @@ void or_quant_x(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* sf, int nt
 /* Forward pass.  tokens == NULL computes every token; otherwise only the
  * ntok listed tokens, with y rows written in list order ([ntok, H]).
  * Optional per-pool-row outputs (only when tokens == NULL; may be NULL):
- *   hq_pool [p_cap, I], hsf_pool [p_cap, I/32], o_pool [p_cap, H] (bf16 bits).
+ *   hq_pool [p_cap, I], hsf_pool [p_cap, I/32], o_pool [p_cap, H] (bf16 bits),
+ *   h_pool [p_cap, I] (fp32 SwiGLU*w before requantisation).
  * Work is done expert by expert over the expert-major pool, each expert's
  * weights dequantised once.  Returns the or_plan status (0 ok). */
 int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
                int T, int k, int E, int H, int I,
                const uint8_t* w1q, const uint8_t* w1sf, const uint8_t* w2q, const uint8_t* w2sf,
                const int32_t* tokens, int ntok, uint16_t* y,
-               uint8_t* hq_pool, uint8_t* hsf_pool, uint16_t* o_pool, int64_t p_cap, int nthreads) {
+               uint8_t* hq_pool, uint8_t* hsf_pool, uint16_t* o_pool, float* h_pool, int64_t p_cap,
+               int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
@@ -363,6 +365,7 @@ int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
                     if (hq_pool) memcpy(hq_pool + (size_t)r * I, hq, (size_t)I);
                     if (hsf_pool) memcpy(hsf_pool + (size_t)r * (I / OR_SF_VEC), hsf, (size_t)I / OR_SF_VEC);
                     if (o_pool) memcpy(o_pool + (size_t)r * H, o, sizeof(uint16_t) * H);
+                    if (h_pool) memcpy(h_pool + (size_t)r * I, h, sizeof(float) * I);
                 }
             }
             free(xd); free(hd); free(h); free(hq); free(hsf); free(o);

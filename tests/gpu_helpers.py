@@ -1,0 +1,83 @@
+"""Shared helpers of the GPU parity tests: build inputs on the device, run the
+oracle on the same bytes, convert tensor-core scale layouts back to
+row-major, and the output tolerance of the layer."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from moe_expert_layer_counts_gb300 import inputs
+
+# Output bar: relative L2 <= 5e-3 and max-abs <= 2e-2 * rms(y_oracle).
+REL_L2 = 5e-3
+MAX_ABS_RMS = 2e-2
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 numpy bits (host)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_values(b: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def setup(moe, w: inputs.Workload, seed: int = 0, idx=None, tw=None):
+    d = inputs.make_inputs(w, seed=seed, device="cuda")
+    if idx is not None:
+        d["topk_idx"] = torch.as_tensor(idx, dtype=torch.int64, device="cuda").contiguous()
+    if tw is not None:
+        d["topk_w"] = torch.as_tensor(tw, dtype=torch.float32, device="cuda").contiguous()
+    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"])
+    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"])
+    return d, W1, W2
+
+
+def host(d):
+    """Numpy copies of the inputs for the oracle."""
+    return dict(x=bits(d["x"]), topk_idx=d["topk_idx"].cpu().numpy(), topk_w=d["topk_w"].cpu().numpy(),
+                w1q=d["w1q"].cpu().numpy(), w1sf=d["w1sf"].cpu().numpy(), w2q=d["w2q"].cpu().numpy(),
+                w2sf=d["w2sf"].cpu().numpy())
+
+
+def oracle_forward(oracle, h, E, tokens=None, want_pool=False):
+    return oracle.forward(h["x"], h["topk_idx"], h["topk_w"], E, h["w1q"], h["w1sf"], h["w2q"], h["w2sf"],
+                          tokens=tokens, want_pool=want_pool)
+
+
+def sf_rows_from_mma(buf: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Tensor-core scale chunks [rows/128][K/128][512] -> row-major [rows, K/32]."""
+    ch = buf[: (rows // 128) * (K // 128) * 512].reshape(rows // 128, K // 128, 512)
+    m = np.arange(128)
+    sub = np.arange(4)
+    pos = (16 * (m % 32) + 4 * (m // 32))[:, None] + sub[None, :]  # [128, 4]
+    out = ch[:, :, pos]                      # [rb, kb, 128, 4]
+    return out.transpose(0, 2, 1, 3).reshape(rows, K // 32)
+
+
+def sf_mma_from_rows(sf: np.ndarray) -> np.ndarray:
+    """Inverse of sf_rows_from_mma."""
+    rows, kq = sf.shape
+    K = kq * 32
+    m = np.arange(128)
+    sub = np.arange(4)
+    pos = (16 * (m % 32) + 4 * (m // 32))[:, None] + sub[None, :]
+    ch = np.zeros((rows // 128, K // 128, 512), np.uint8)
+    src = sf.reshape(rows // 128, 128, K // 128, 4).transpose(0, 2, 1, 3)  # [rb, kb, 128, 4]
+    ch[:, :, pos] = src
+    return ch.reshape(-1)
+
+
+def assert_close_output(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: str = "y"):
+    a = bf16_values(y_gpu_bits)
+    b = bf16_values(y_ref_bits)
+    assert np.all(np.isfinite(a)), f"{what}: non-finite GPU output"
+    nrm = np.linalg.norm(b)
+    rel = np.linalg.norm(a - b) / max(nrm, 1e-30)
+    rms = np.sqrt(np.mean(b * b)) if b.size else 0.0
+    mx = np.max(np.abs(a - b)) if a.size else 0.0
+    assert rel <= REL_L2 or nrm == 0, f"{what}: relative L2 {rel:.3e} > {REL_L2}"
+    assert mx <= MAX_ABS_RMS * rms or nrm == 0, f"{what}: max-abs {mx:.3e} > {MAX_ABS_RMS} * rms {rms:.3e}"
+    if nrm == 0:
+        assert np.all(a == 0), f"{what}: oracle output is zero, GPU output is not"
+    return rel, mx / max(rms, 1e-30)

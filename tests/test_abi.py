@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads and exports every symbol include/moe.h
+declares; host-only entry points answer without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libmoe():
+    from moe_expert_layer_counts_gb300 import build as b
+    b.build()
+    return ctypes.CDLL(b.LIB)
+
+
+def header_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            txt = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+            names |= set(re.findall(r"^\s*(?:size_t|int|const char\*)\s+(moe_\w+)\s*\(", txt, flags=re.M))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(libmoe):
+    import moe_expert_layer_counts_gb300 as m
+    names = header_functions()
+    assert len(names) >= 12
+    assert set(names) == set(m.SYMBOLS)
+    for n in names:
+        assert hasattr(libmoe, n), n
+
+
+def test_host_only_sizes(libmoe):
+    f = libmoe.moe_plan_workspace_bytes
+    f.restype = ctypes.c_size_t
+    full = f(8192, 8, 256, 7168, 2048)
+    assert full > 2 * 10 ** 9
+    assert f(0, 8, 256, 7168, 2048) > 0          # empty batch is valid
+    assert f(64, 2, 8, 256, 128) < full
+    for bad in [(64, 0, 8, 256, 128), (64, 33, 8, 256, 128), (64, 2, 0, 256, 128), (64, 2, 2000, 256, 128),
+                (64, 2, 8, 200, 128), (64, 2, 8, 256, 100), (-1, 2, 8, 256, 128)]:
+        assert f(*bad) == 0, bad
+    g = libmoe.moe_weight_scales_bytes
+    g.restype = ctypes.c_size_t
+    assert g(256, 4096, 7168) == 256 * 32 * 56 * 512
+    assert g(1, 100, 128) == 0
+
+
+def test_argument_errors_before_any_device_call(libmoe):
+    libmoe.moe_plan.restype = ctypes.c_int
+    libmoe.moe_plan.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_size_t,
+                                                                               ctypes.c_void_p]
+    assert libmoe.moe_plan(None, None, None, 4, 2, 8, 256, 128, None, 0, None) == 1  # MOE_ERR_INVALID_ARG
+    plan = ctypes.create_string_buffer(192)
+    # misaligned workspace pointer
+    assert libmoe.moe_plan(plan, 16, 16, 4, 2, 8, 256, 128, 8, 1 << 30, None) == 1
+    # unsupported shape
+    assert libmoe.moe_plan(plan, 16, 16, 4, 2, 8, 200, 128, 256, 1 << 30, None) == 2
+    # workspace too small
+    assert libmoe.moe_plan(plan, 16, 16, 4, 2, 8, 256, 128, 256, 16, None) == 3
+    libmoe.moe_forward.restype = ctypes.c_int
+    libmoe.moe_forward.argtypes = [ctypes.c_void_p] * 6
+    assert libmoe.moe_forward(None, None, None, plan, None, None) == 1  # plan never filled
+    libmoe.moe_error_string.restype = ctypes.c_char_p
+    for s in range(8):
+        assert libmoe.moe_error_string(s)

@@ -1,0 +1,113 @@
+"""End-to-end GPU forward against the oracle: all rows on the small
+workloads, sampled tokens at full size, and the degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as gh
+from moe_expert_layer_counts_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run(moe, w, d, W1, W2):
+    p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I)
+    y = moe.forward(d["x"], W1, W2, p)
+    return p, y
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_forward_all_tokens(moe, oracle, name):
+    w = inputs.WORKLOADS[name]
+    d, W1, W2 = gh.setup(moe, w)
+    p, y = run(moe, w, d, W1, W2)
+    assert moe.plan_check(p) == 0
+    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
+    gh.assert_close_output(gh.bits(y), ref["y"], name)
+
+
+@pytest.mark.parametrize("name", ["share", "full", "decode"])
+def test_forward_sampled_tokens_full_size(moe, oracle, name):
+    w = inputs.WORKLOADS[name]
+    d, W1, W2 = gh.setup(moe, w)
+    p, y = run(moe, w, d, W1, W2)
+    assert moe.plan_check(p) == 0
+    h = gh.host(d)
+    rng = np.random.default_rng(0)
+    toks = np.unique(np.concatenate([[0, 1, w.T - 1], rng.choice(w.T, 29, replace=False)])).astype(np.int32)
+    if name == "share":  # include tokens with no local expert (y must be 0)
+        none = np.nonzero((h["topk_idx"] < 0).all(1))[0][:3]
+        toks = np.unique(np.concatenate([toks, none])).astype(np.int32)
+    ref = gh.oracle_forward(oracle, h, w.E, tokens=toks)
+    yb = gh.bits(y)[toks]
+    gh.assert_close_output(yb, ref["y"], name)
+    if name == "share":
+        for t in np.nonzero((h["topk_idx"][toks] < 0).all(1))[0]:
+            assert np.all(yb[t] == 0)
+    # output rows are finite everywhere
+    assert torch.isfinite(y.float()).all()
+
+
+def test_forward_deterministic(moe):
+    w = inputs.WORKLOADS["mid"]
+    d, W1, W2 = gh.setup(moe, w)
+    _, y1 = run(moe, w, d, W1, W2)
+    _, y2 = run(moe, w, d, W1, W2)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_forward_edge_routings(moe, oracle):
+    w = inputs.Workload("edge", 512, 256, 128, 8, 4, "uniform")
+    rng = np.random.default_rng(3)
+    cases = {}
+    # one expert gets every entry (duplicates inside a token)
+    cases["one_expert"] = np.full((w.T, w.k), 3)
+    # experts with 0, 1, 127, 128, 129 rows
+    flat = np.concatenate([np.full(n, e) for e, n in {1: 1, 2: 127, 3: 128, 4: 129}.items()])
+    flat = np.concatenate([flat, np.full(w.T * w.k - flat.size, -1)])
+    cases["ragged"] = rng.permutation(flat).reshape(w.T, w.k)
+    # all entries skipped
+    cases["none"] = -np.ones((w.T, w.k))
+    for name, idx in cases.items():
+        tw = rng.random((w.T, w.k)).astype(np.float32)
+        d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
+        p, y = run(moe, w, d, W1, W2)
+        assert moe.plan_check(p) == 0
+        ref = gh.oracle_forward(oracle, gh.host(d), w.E)
+        gh.assert_close_output(gh.bits(y), ref["y"], name)
+        if name == "none":
+            assert torch.all(y.view(torch.int16) == 0)
+
+
+def test_bad_expert_ids_reported(moe, oracle):
+    w = inputs.WORKLOADS["tiny"]
+    idx, tw = inputs.make_routing(w)
+    idx = idx.clone()
+    idx[5, 1] = w.E          # out of range: skipped and reported
+    idx[9, 0] = -3
+    d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
+    p, y = run(moe, w, d, W1, W2)
+    assert moe.plan_check(p) == moe.ERR_BAD_EXPERT_ID
+    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
+    gh.assert_close_output(gh.bits(y), ref["y"], "bad ids")
+
+
+def test_empty_batch_forward(moe):
+    w = inputs.Workload("empty", 0, 256, 128, 8, 2, "uniform")
+    d, W1, W2 = gh.setup(moe, inputs.Workload("w", 4, 256, 128, 8, 2, "uniform"))
+    idx = torch.zeros(0, 2, dtype=torch.int64, device="cuda")
+    tw = torch.zeros(0, 2, dtype=torch.float32, device="cuda")
+    p = moe.plan(idx, tw, w.E, w.H, w.I)
+    y = torch.empty(0, w.H, dtype=torch.bfloat16, device="cuda")
+    moe.forward(torch.empty(0, w.H, dtype=torch.bfloat16, device="cuda"), W1, W2, p, y)
+    assert moe.plan_check(p) == 0
+
+
+def test_odd_h_tail_tile(moe, oracle):
+    """H = 384: the last L2 output tile holds 128 valid columns of 256."""
+    w = inputs.Workload("oddH", 96, 384, 256, 4, 2, "uniform")
+    d, W1, W2 = gh.setup(moe, w)
+    p, y = run(moe, w, d, W1, W2)
+    assert moe.plan_check(p) == 0
+    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
+    gh.assert_close_output(gh.bits(y), ref["y"], "oddH")
