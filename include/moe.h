@@ -52,7 +52,8 @@ typedef enum moe_status {
     MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     MOE_ERR_BAD_EXPERT_ID = 5, /* device saw topk_idx outside [-1, E); those entries were skipped */
     MOE_ERR_TIMEOUT = 6,       /* a bounded device-side wait expired; outputs are invalid */
-    MOE_ERR_NO_KERNEL = 7      /* the library holds no code for this device */
+    MOE_ERR_NO_KERNEL = 7,     /* the library holds no code for this device */
+    MOE_ERR_TOO_LARGE = 8      /* sizes exceed the fixed scratch of moe_expert_offsets_static() */
 } moe_status;
 
 /* Rows of one MMA tile; every expert's pool segment is padded to it
@@ -171,6 +172,34 @@ enum {
     MOE_EXPORT_POOL_ROWS = 15    /* (size only) P_cap, the pool row capacity, in the size field */
 };
 int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* bytes);
+
+/* Expert counts and offsets for callers that cannot allocate device memory.
+ * The analysed pages have no counterpart of this entry point.
+ *
+ * Some callers cannot call cudaMalloc at all: a plugin that runs inside a
+ * host framework which owns every byte of device memory, or a serving loop
+ * whose memory budget is frozen after start-up (an allocation there may also
+ * synchronise the device).  Such callers can still pass their inputs and
+ * outputs, but not a workspace.  This entry point runs the same counting and
+ * prefix-sum kernels as moe_plan(), with their scratch (per-chunk
+ * histograms, per-chunk bases, the row-block table) in a fixed array inside
+ * the library: about 280 KB of device memory that every GPU which loads the
+ * library keeps until the process exits.  Nothing is allocated per call.
+ *   topk_idx        [T, k] int64 (device); -1 = not routed; other ids outside
+ *                   [-1, E) are skipped (not reported here)
+ *   count           out [E] int32 (device): entries per expert
+ *   offsets         out [E+1] int32 (device): exclusive scan of count
+ *   padded_offsets  out [E+1] int32 (device): exclusive scan of count rounded
+ *                   up to MOE_BLOCK_M
+ * Limits: T*k <= 262144, E <= 1024, ceil(T*k / 2048) * E <= 32768, 1 <= k <= 32;
+ * larger sizes return MOE_ERR_TOO_LARGE before anything is enqueued.
+ * The first call on a device looks up the array's device address (a CUDA
+ * runtime query, no allocation); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents, so calls whose kernels overlap on the GPU (different streams
+ * without ordering) race and give wrong results; order them on one stream. */
+int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, int E, int32_t* count, int32_t* offsets,
+                              int32_t* padded_offsets, void* stream);
 
 /* Static text for a status code. */
 const char* moe_error_string(int status);

@@ -32,6 +32,7 @@ ERR_WORKSPACE = 3
 ERR_CUDA = 4
 ERR_BAD_EXPERT_ID = 5
 ERR_TIMEOUT = 6
+ERR_TOO_LARGE = 8
 
 EXPORT = dict(count=0, off=1, poff=2, slot_of=3, row_token=4, row_topk=5, row_weight=6, block_expert=7,
               n_blocks=8, pool_q=9, pool_sf=10, h_q=11, h_sf=12, l2_out=13, error=14, pool_rows=15)
@@ -43,7 +44,7 @@ _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_
 # every function declared in include/moe.h
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",
            "moe_dispatch", "moe_expert_l1", "moe_expert_l2", "moe_combine", "moe_forward", "moe_plan_check",
-           "moe_plan_export", "moe_error_string")
+           "moe_plan_export", "moe_error_string", "moe_expert_offsets_static")
 
 
 class MoeError(RuntimeError):
@@ -92,6 +93,8 @@ def lib():
             L.moe_plan_check.argtypes = [ctypes.POINTER(Plan), P]
             L.moe_plan_export.restype = i32
             L.moe_plan_export.argtypes = [ctypes.POINTER(Plan), i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+            L.moe_expert_offsets_static.restype = i32
+            L.moe_expert_offsets_static.argtypes = [P, i32, i32, i32, P, P, P, P]
             L.moe_error_string.restype = ctypes.c_char_p
             L.moe_error_string.argtypes = [i32]
             _lib = L
@@ -224,3 +227,18 @@ def forward(x: torch.Tensor, W1: MXFP4Weight, W2: MXFP4Weight, p: MoePlan, y: to
 def plan_check(p: MoePlan, stream=None) -> int:
     """Synchronise and return the device-side status (0, ERR_BAD_EXPERT_ID, ERR_TIMEOUT)."""
     return int(lib().moe_plan_check(ctypes.byref(p.c), _stream(stream)))
+
+
+def expert_offsets_static(topk_idx: torch.Tensor, E: int, stream=None):
+    """moe_expert_offsets_static: (count [E], offsets [E+1], padded offsets [E+1]) int32,
+    computed with the library's fixed scratch instead of a caller workspace.  Only the
+    three outputs are allocated here (by torch); the C entry point allocates nothing."""
+    T, k = topk_idx.shape
+    assert topk_idx.dtype == torch.int64
+    topk_idx = topk_idx.contiguous()
+    count = torch.empty(E, dtype=torch.int32, device=topk_idx.device)
+    off = torch.empty(E + 1, dtype=torch.int32, device=topk_idx.device)
+    poff = torch.empty(E + 1, dtype=torch.int32, device=topk_idx.device)
+    _check(lib().moe_expert_offsets_static(_ptr(topk_idx), T, k, E, _ptr(count), _ptr(off), _ptr(poff),
+                                           _stream(stream)), "moe_expert_offsets_static")
+    return count, off, poff

@@ -284,6 +284,9 @@ const char* moe_error_string(int status) {
         case MOE_ERR_BAD_EXPERT_ID: return "topk_idx held an expert id outside [-1, E); those entries were skipped";
         case MOE_ERR_TIMEOUT: return "a bounded device-side wait expired; outputs are invalid";
         case MOE_ERR_NO_KERNEL: return "no kernel image for this device";
+        case MOE_ERR_TOO_LARGE:
+            return "sizes exceed the fixed scratch of moe_expert_offsets_static (T*k <= 262144, E <= 1024, "
+                   "ceil(T*k/2048)*E <= 32768)";
         default: return "unknown status";
     }
 }

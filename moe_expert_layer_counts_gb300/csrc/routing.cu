@@ -216,3 +216,69 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Expert counts and offsets without a caller workspace.  The scratch of the
+// count and scan kernels lives in one fixed device array of this file; its
+// device address is looked up once per device (host code may not use the
+// array's name as an address).
+namespace moe {
+namespace {
+
+constexpr int64_t kStaticMaxEntries = 262144;   // T * k
+constexpr int kStaticMaxChunkExperts = 32768;   // ceil(T*k / kRouteChunk) * E
+constexpr int kStaticBlockCap = 4096;           // row blocks: (262144 + 1024*127) / 128 < 4096
+constexpr int kStaticHist = 0;
+constexpr int kStaticBase = kStaticMaxChunkExperts;
+constexpr int kStaticBlocks = 2 * kStaticMaxChunkExperts;
+constexpr int kStaticNBlocks = kStaticBlocks + kStaticBlockCap;
+constexpr int kStaticErr = kStaticNBlocks + 32;
+constexpr int kStaticInts = kStaticErr + 32;
+
+static __device__ __align__(256) int g_offsets_scratch[kStaticInts];
+
+int* static_scratch_ptr(int dev) {
+    static int* ptrs[64] = {};
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_offsets_scratch) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, int E, int32_t* count,
+                                         int32_t* offsets, int32_t* padded_offsets, void* stream) {
+    using namespace moe;
+    if (T < 0 || k < 1 || k > kMaxTopk || E < 1) return MOE_ERR_INVALID_ARG;
+    if (!count || !offsets || !padded_offsets || (T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
+    const int64_t n = static_cast<int64_t>(T) * k;
+    const int chunks = static_cast<int>((n + kRouteChunk - 1) / kRouteChunk);
+    if (E > kMaxExperts || n > kStaticMaxEntries || static_cast<int64_t>(chunks) * E > kStaticMaxChunkExperts)
+        return MOE_ERR_TOO_LARGE;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (!(major == 10 && minor == 3)) return MOE_ERR_UNSUPPORTED;
+    int* scratch = static_scratch_ptr(dev);
+    if (!scratch) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the error word is the only scratch that must start at zero; the count
+    // and scan kernels overwrite every other word they read
+    if (cudaMemsetAsync(scratch + kStaticErr, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (chunks > 0) {
+        route_count_kernel<<<chunks, kCountThreads, E * sizeof(int), s>>>(topk_idx, n, E, scratch + kStaticHist,
+                                                                          scratch + kStaticErr);
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    route_scan_kernel<<<1, kScanThreads, 0, s>>>(scratch + kStaticHist, chunks, E, count, offsets, padded_offsets,
+                                                 scratch + kStaticBase, scratch + kStaticBlocks,
+                                                 scratch + kStaticNBlocks);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
