@@ -224,6 +224,9 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     n_valid = int((d["topk_idx"] >= 0).sum().item())
     flops = 6.0 * n_valid * w.H * w.I
+    # weight bytes the step must stream: FP4 codes + UE8M0 scales of every touched expert (W1 and W2)
+    touched = int(torch.unique(d["topk_idx"][d["topk_idx"] >= 0]).numel())
+    weight_bytes = touched * 3 * w.H * w.I * (0.5 + 1.0 / 32)
 
     def step(ev=None):
         if ev: ev[0].record()
@@ -310,6 +313,11 @@ def main():
                     k=w.k, valid_entries=n_valid, l2="flushed before every timed step (512 MB write)",
                     parallelism=f"replicas x{world}"),
         tokens_per_s=world * w.T * args.steps / t_max,
+        weight_stream=dict(touched_experts=touched, bytes_per_step=weight_bytes,
+                           gbs=weight_bytes / (t_max / args.steps) / 1e9,
+                           pct_hbm=weight_bytes / (t_max / args.steps) / 1e9 / pk["hbm_gbs"],
+                           note=f"touched experts' FP4 + UE8M0 weight bytes per step / step time, vs {pk['source']} "
+                                f"HBM copy bandwidth {pk['hbm_gbs']} GB/s"),
         pct_fp8_peak=value / fp8_sus,
         fp8_peak_tflops=dict(value=fp8_sus, note=f"2 x {pk['source']} sustained bf16 cuBLAS rate"),
         stage_ms={s: v / args.steps for s, v in stage_ms.items()},

@@ -293,35 +293,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool go = !aborted(sh) && wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p.err, 48);
             if (!__all_sync(0xffffffffu, go)) break;
             ptx::tc_fence_after();
-            // Drain this warp's half of the accumulator row into registers as
-            // packed bf16 pairs and release tensor memory at once, so the next
-            // tile's MMAs overlap the rest of the epilogue.  (Layer 1 rounds
-            // gate/up to bf16 here anyway; layer 2 rounds its output to bf16.)
+            // Drain this warp's half of the accumulator row into registers with
+            // wide loads and release tensor memory at once, so the next tile's
+            // MMAs start while this epilogue converts and stores.
             uint32_t pk[64];
             if (kLayer == 1) {
+                uint32_t g[64], u[64];
+                ptx::tmem_ld_32x32b_x64(t_row + 64 * half, g);
+                ptx::tmem_ld_32x32b_x64(t_row + 128 + 64 * half, u);
+                ptx::tc_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
+                // gate/up rounded to bf16 (the reading of the pages' bf16 gate/up)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t g[16], u[16];
-                    ptx::tmem_ld_32x32b_x16(t_row + 64 * half + 16 * c, g);
-                    ptx::tmem_ld_32x32b_x16(t_row + 128 + 64 * half + 16 * c, u);
-                    ptx::tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[16 * c + i] = bf16x2_rn(__uint_as_float(g[i]), __uint_as_float(u[i]));
-                }
+                for (int i = 0; i < 64; ++i) pk[i] = bf16x2_rn(__uint_as_float(g[i]), __uint_as_float(u[i]));
             } else {
+                uint32_t v[128];
+                ptx::tmem_ld_32x32b_x128(t_row + 128 * half, v);
+                ptx::tc_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(t_row + 128 * half + 32 * c, v);
-                    ptx::tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        pk[16 * c + i] = bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                }
+                for (int i = 0; i < 64; ++i) pk[i] = bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
             if (tok >= 0) {
                 if (kLayer == 1) {
                     // intermediate columns j*128 + 64*half + [0, 64): two 32-blocks
