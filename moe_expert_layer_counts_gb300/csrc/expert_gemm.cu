@@ -106,38 +106,67 @@ __device__ __noinline__ float silu_exact(float g) {
 // snippets).  gu holds (bf16 gate, bf16 up) pairs.  The fast path uses
 // __expf and an approximate divide (error well below kDecisionUlps for
 // |gate| <= 16).  Wherever that could change an integer decision under the
-// exact formula, the exact value is used instead: an element within
-// kDecisionUlps of an E4M3 code midpoint (or with |gate| > 16) is recomputed
+// exact formula, the exact value is used instead: an element with
+// |gate| > 16 or within kDecisionUlps of an E4M3 code midpoint is recomputed
 // alone; if the block maximum lies that close to the UE8M0 scale boundary,
 // the whole block is recomputed.  So every code and scale byte is the one the
-// exact definition gives.  Writes 32 E4M3 codes to dst (16-byte aligned) and
-// returns the scale byte.
+// exact definition gives.  The fast path is branch-free (it only collects
+// bit masks), so the 32 values are computed with full instruction-level
+// parallelism.  Writes 32 E4M3 codes to dst (16-byte aligned) and returns the
+// scale byte.
 constexpr uint32_t kDecisionUlps = 64;
 
+// Replace h[i] by its exact value for every bit i set in `mask` (rare; a
+// local copy keeps dynamic indexing off the fast path).
+__device__ __noinline__ void exact_fixup(const uint32_t* gu, float wgt, float* h, uint32_t mask) {
+    while (mask) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1;
+        h[i] = (silu_exact(bf16_lo(gu[i])) * bf16_hi(gu[i])) * wgt;
+    }
+}
+
+__device__ __forceinline__ void fixup(const uint32_t* gu, float wgt, float (&h)[32], uint32_t mask) {
+    uint32_t gl[32];
+    float hl[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        gl[i] = gu[i];
+        hl[i] = h[i];
+    }
+    exact_fixup(gl, wgt, hl, mask);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) h[i] = hl[i];
+}
+
 __device__ __forceinline__ uint32_t requant_block(const uint32_t* gu, float wgt, uint8_t* dst) {
+    // 1. fast path, straight-line: values, block maximum, values it cannot decide
     float h[32];
-    float amax = 0.0f;
+    uint32_t big = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const float g = bf16_lo(gu[i]), u = bf16_hi(gu[i]);
-        const float silu = fabsf(g) > 16.0f ? silu_exact(g) : __fdividef(g, 1.0f + __expf(-g));
-        h[i] = (silu * u) * wgt;
-        amax = fmaxf(amax, fabsf(h[i]));
+        h[i] = (__fdividef(g, 1.0f + __expf(-g)) * u) * wgt;
+        big |= static_cast<uint32_t>(fabsf(g) > 16.0f) << i;
     }
+    if (big) fixup(gu, wgt, h, big);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    // 2. the scale: if the maximum sits near the boundary, the whole block goes exact
     if (near_e4m3_scale_boundary(amax, kDecisionUlps)) {
+        fixup(gu, wgt, h, 0xFFFFFFFFu);
         amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            h[i] = (silu_exact(bf16_lo(gu[i])) * bf16_hi(gu[i])) * wgt;
-            amax = fmaxf(amax, fabsf(h[i]));
-        }
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
     }
     const uint32_t sbyte = ue8m0_scale_e4m3(amax);
     const float inv = inv_scale_from_byte(sbyte);
+    // 3. the codes: values near a rounding midpoint go exact
+    uint32_t near = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (near_e4m3_midpoint(h[i] * inv, kDecisionUlps))
-            h[i] = (silu_exact(bf16_lo(gu[i])) * bf16_hi(gu[i])) * wgt;
+    for (int i = 0; i < 32; ++i) near |= static_cast<uint32_t>(near_e4m3_midpoint(h[i] * inv, kDecisionUlps)) << i;
+    if (near) fixup(gu, wgt, h, near);
     uint32_t q[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -191,9 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
         const int nb_per_expert = p.N / 128;
-        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-            const int b = w / p.n_tiles, j = w % p.n_tiles;
-            const int e = __ldg(p.block_expert + b);
+        // operand coordinates of work item w
+        struct Tile {
+            int b, row_b0, row_b1;
+            bool b1_in_range;
+            const uint8_t *sfa, *sfb0, *sfb1;
+        };
+        auto tile_of = [&](int w) {
+            Tile t;
+            t.b = w / p.n_tiles;
+            const int j = w % p.n_tiles;
+            const int e = __ldg(p.block_expert + t.b);
             int nb0, nb1;
             if (kLayer == 1) {
                 nb0 = j;                       // gate rows j*128..
@@ -202,11 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 nb0 = 2 * j;
                 nb1 = min(2 * j + 1, nb_per_expert - 1);  // tail tile of an odd H/128: re-read, ignored
             }
-            const int row_b0 = e * p.N + nb0 * 128;
-            const int row_b1 = e * p.N + (kLayer == 1 ? nb1 * 128 : (2 * j + 1) * 128);
-            const uint8_t* sfb0 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb0) * kb_count * kSfChunkBytes;
-            const uint8_t* sfb1 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb1) * kb_count * kSfChunkBytes;
-            const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
+            t.row_b0 = e * p.N + nb0 * 128;
+            t.row_b1 = e * p.N + (kLayer == 1 ? nb1 * 128 : (2 * j + 1) * 128);
+            t.b1_in_range = kLayer == 1 || 2 * j + 1 < nb_per_expert;
+            t.sfb0 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb0) * kb_count * kSfChunkBytes;
+            t.sfb1 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb1) * kb_count * kSfChunkBytes;
+            t.sfa = p.sfa + static_cast<size_t>(t.b) * kb_count * kSfChunkBytes;
+            return t;
+        };
+        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+            const Tile t = tile_of(w);
             for (int kb = 0; kb < kb_count; ++kb) {
                 if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
                     ok = false;
@@ -215,12 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* st = smem + stage * kStageStride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
                 ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a, kb * kBlockK, b * kBlockM, full);
-                ptx::tma_load_2d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, row_b0, full);
-                ptx::tma_load_2d(ptx::smem_addr(st + kABytes + kBBoxBytes), &tmap_b, kb * kBlockK, row_b1, full);
-                ptx::bulk_load(ptx::smem_addr(st + kSfaOff), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
-                ptx::bulk_load(ptx::smem_addr(st + kSfbOff), sfb0 + kb * kSfChunkBytes, kSfChunkBytes, full);
-                ptx::bulk_load(ptx::smem_addr(st + kSfbOff + kSfChunkBytes), sfb1 + kb * kSfChunkBytes,
+                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a, kb * kBlockK, t.b * kBlockM, full);
+                ptx::tma_load_2d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, t.row_b0, full);
+                ptx::tma_load_2d(ptx::smem_addr(st + kABytes + kBBoxBytes), &tmap_b, kb * kBlockK, t.row_b1, full);
+                ptx::bulk_load(ptx::smem_addr(st + kSfaOff), t.sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
+                ptx::bulk_load(ptx::smem_addr(st + kSfbOff), t.sfb0 + kb * kSfChunkBytes, kSfChunkBytes, full);
+                ptx::bulk_load(ptx::smem_addr(st + kSfbOff + kSfChunkBytes), t.sfb1 + kb * kSfChunkBytes,
                                kSfChunkBytes, full);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
