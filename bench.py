@@ -217,8 +217,8 @@ def main():
     import moe_expert_layer_counts_gb300 as moe
     dev = torch.device("cuda", torch.cuda.current_device())
     d = inputs.make_inputs(w, seed=0, device=dev)
-    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"])
-    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"])
+    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"], layer=1)
+    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"], layer=2)
     ws = moe.alloc_workspace(w.T, w.k, w.E, w.H, w.I, dev)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)

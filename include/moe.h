@@ -72,7 +72,8 @@ typedef struct moe_plan_t {
  *   q       e2m1 codes, two per byte, the even K index in the low nibble,
  *           bit 3 of a nibble = sign; [E][N][K/2] bytes, 32-byte aligned.
  *   sf_mma  UE8M0 scales (biased exponents, one per 32 along K) in the
- *           tensor-core layout written by moe_prepare_weight_scales().
+ *           tensor-core layout written by moe_prepare_weight_scales()
+ *           (MOE_SF_PAIRS_HALVES for W1, MOE_SF_PAIRS_ADJACENT for W2).
  * W1 has N = 2I (gate rows 0..I-1, then up rows I..2I-1), K = H.
  * W2 has N = H, K = I. */
 typedef struct moe_weights_t {
@@ -86,17 +87,30 @@ typedef struct moe_weights_t {
  * output.  Returns 0 if the shapes are unsupported.  Host-only, no CUDA. */
 size_t moe_plan_workspace_bytes(int T, int k, int E, int H, int I);
 
-/* Bytes of the tensor-core scale layout for an [E, N, K] weight.  0 if
- * N % 128 or K % 128 is nonzero.  Host-only. */
+/* Bytes of the tensor-core scale layout for an [E, N, K] weight:
+ * E * ceil(N/256) * (K/128) * 1024.  0 if N % 128 or K % 128 is nonzero.
+ * Host-only. */
 size_t moe_weight_scales_bytes(int E, int N, int K);
+
+/* How moe_prepare_weight_scales pairs 128-row chunks: the expert GEMMs read
+ * one pair per 256-row weight tile, so both chunks of a pair, for every 128-K
+ * step, are stored side by side. */
+enum {
+    MOE_SF_PAIRS_ADJACENT = 0, /* pair p = rows [256p, 256p+256) (W2) */
+    MOE_SF_PAIRS_HALVES = 1    /* pair p = rows [128p, +128) and [N/2 + 128p, +128) (W1: gate | up) */
+};
 
 /* One-time relayout of weight scales (not part of the per-batch path; the
  * pages' "transformed_l1_weights" plays the same role).
- *   sf      UE8M0 bytes [E][N][K/32] (device, row-major)
- *   sf_mma  output, moe_weight_scales_bytes(E,N,K) bytes (device)
- * Errors: MOE_ERR_INVALID_ARG (null pointers, small buffer),
- * MOE_ERR_UNSUPPORTED (N or K not multiples of 128), MOE_ERR_CUDA. */
-int moe_prepare_weight_scales(const void* sf, int E, int N, int K, void* sf_mma,
+ *   sf       UE8M0 bytes [E][N][K/32] (device, row-major)
+ *   pairing  MOE_SF_PAIRS_HALVES for W1, MOE_SF_PAIRS_ADJACENT for W2
+ *   sf_mma   output, moe_weight_scales_bytes(E,N,K) bytes (device); layout
+ *            [E][pair][K/128][2][512], each 512-byte chunk holding 128 rows x
+ *            4 scales at byte 16*(row%32) + 4*(row/32) + (k/32)%4
+ * Errors: MOE_ERR_INVALID_ARG (null pointers, small buffer, bad pairing, N/2
+ * not a multiple of 128 for MOE_SF_PAIRS_HALVES), MOE_ERR_UNSUPPORTED (N or K
+ * not multiples of 128), MOE_ERR_CUDA. */
+int moe_prepare_weight_scales(const void* sf, int E, int N, int K, int pairing, void* sf_mma,
                               size_t sf_mma_bytes, void* stream);
 
 /* Dispatch plan (DeepEP -> Mega MoE page, dispatch.cuh snippet: expert count,

@@ -33,6 +33,8 @@ ERR_CUDA = 4
 ERR_BAD_EXPERT_ID = 5
 ERR_TIMEOUT = 6
 ERR_TOO_LARGE = 8
+SF_PAIRS_ADJACENT = 0
+SF_PAIRS_HALVES = 1
 
 EXPORT = dict(count=0, off=1, poff=2, slot_of=3, row_token=4, row_topk=5, row_weight=6, block_expert=7,
               n_blocks=8, pool_q=9, pool_sf=10, h_q=11, h_sf=12, l2_out=13, error=14, pool_rows=15)
@@ -78,7 +80,7 @@ def lib():
             L.moe_weight_scales_bytes.restype = sz
             L.moe_weight_scales_bytes.argtypes = [i32] * 3
             L.moe_prepare_weight_scales.restype = i32
-            L.moe_prepare_weight_scales.argtypes = [P, i32, i32, i32, P, sz, P]
+            L.moe_prepare_weight_scales.argtypes = [P, i32, i32, i32, i32, P, sz, P]
             L.moe_plan.restype = i32
             L.moe_plan.argtypes = [ctypes.POINTER(Plan), P, P, i32, i32, i32, i32, i32, P, sz, P]
             for name in ("moe_dispatch", "moe_combine"):
@@ -138,8 +140,10 @@ class MXFP4Weight:
         self.c = Weights(q.data_ptr(), sf_mma.data_ptr(), E, N, K)
 
     @classmethod
-    def prepare(cls, q: torch.Tensor, sf: torch.Tensor, stream=None) -> "MXFP4Weight":
-        """q: uint8 [E,N,K/2] packed e2m1; sf: uint8 [E,N,K/32]; both on the GPU."""
+    def prepare(cls, q: torch.Tensor, sf: torch.Tensor, layer: int, stream=None) -> "MXFP4Weight":
+        """q: uint8 [E,N,K/2] packed e2m1; sf: uint8 [E,N,K/32]; both on the GPU.
+        layer 1 = W1 (gate rows then up rows), layer 2 = W2."""
+        assert layer in (1, 2)
         E, N, K2 = q.shape
         K = 2 * K2
         assert sf.shape == (E, N, K // 32) and q.is_cuda and sf.is_cuda
@@ -149,7 +153,8 @@ class MXFP4Weight:
         if nbytes == 0:
             raise MoeError(ERR_UNSUPPORTED, "weight_scales_bytes")
         out = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
-        _check(lib().moe_prepare_weight_scales(_ptr(sf), E, N, K, _ptr(out), nbytes, _stream(stream)),
+        pairing = SF_PAIRS_HALVES if layer == 1 else SF_PAIRS_ADJACENT
+        _check(lib().moe_prepare_weight_scales(_ptr(sf), E, N, K, pairing, _ptr(out), nbytes, _stream(stream)),
                "moe_prepare_weight_scales")
         return cls(q, out, E, N, K)
 

@@ -42,9 +42,12 @@ int device_info(int* sms) {
     return MOE_OK;
 }
 
-// Scale relayout: canonical [E][N][K/32] -> chunks [E][N/128][K/128] of 512
-// bytes, byte 16*(n%32) + 4*((n%128)/32) + (k/32)%4.
-__global__ void prepare_sf_kernel(const uint8_t* __restrict__ sf, int64_t total, int N, int K,
+// Scale relayout: canonical [E][N][K/32] -> [E][pair][K/128][2][512]; within
+// a 512-byte chunk (128 rows x 4 scales) byte 16*(n%32) + 4*((n%128)/32) +
+// (k/32)%4.  Pairs: adjacent 128-row chunks (2p, 2p+1), or the chunk p of
+// each half of N (gate | up).  The second chunk of a last, odd adjacent pair
+// stays zero.
+__global__ void prepare_sf_kernel(const uint8_t* __restrict__ sf, int64_t total, int N, int K, int halves,
                                   uint8_t* __restrict__ out) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= total) return;
@@ -53,8 +56,20 @@ __global__ void prepare_sf_kernel(const uint8_t* __restrict__ sf, int64_t total,
     const int kq = static_cast<int>(i % kq_n);
     const int64_t e = row / N;
     const int n = static_cast<int>(row % N);
-    const int nb = n / 128, m = n % 128, kb = kq / 4, sub = kq % 4;
-    const size_t chunk = (static_cast<size_t>(e) * (N / 128) + nb) * (K / 128) + kb;
+    const int pairs = (N + 255) / 256;
+    int pair, half, m;
+    if (halves) {
+        half = n >= N / 2;
+        const int nh = n - half * (N / 2);
+        pair = nh / 128;
+        m = nh % 128;
+    } else {
+        pair = n / 256;
+        half = (n / 128) % 2;
+        m = n % 128;
+    }
+    const int kb = kq / 4, sub = kq % 4;
+    const size_t chunk = ((static_cast<size_t>(e) * pairs + pair) * (K / 128) + kb) * 2 + half;
     out[chunk * kSfChunkBytes + 16 * (m % 32) + 4 * (m / 32) + sub] = sf[i];
 }
 
@@ -118,12 +133,15 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
     return true;
 }
 
-cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, uint8_t* out, cudaStream_t s) {
+cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves, uint8_t* out, size_t out_bytes,
+                              cudaStream_t s) {
     const int64_t total = static_cast<int64_t>(E) * N * (K / kSfVec);
     if (total == 0) return cudaSuccess;
+    cudaError_t st = cudaMemsetAsync(out, 0, out_bytes, s);  // zero the unused half of an odd last pair
+    if (st != cudaSuccess) return st;
     const int threads = 256;
     prepare_sf_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0, s>>>(sf, total, N, K,
-                                                                                                 out);
+                                                                                                 halves, out);
     return cudaGetLastError();
 }
 
@@ -140,19 +158,21 @@ size_t moe_plan_workspace_bytes(int T, int k, int E, int H, int I) {
 
 size_t moe_weight_scales_bytes(int E, int N, int K) {
     if (E < 1 || N < 128 || K < 128 || N % 128 || K % 128) return 0;
-    return static_cast<size_t>(E) * (N / 128) * (K / 128) * kSfChunkBytes;
+    return static_cast<size_t>(E) * ((N + 255) / 256) * (K / 128) * 2 * kSfChunkBytes;
 }
 
-int moe_prepare_weight_scales(const void* sf, int E, int N, int K, void* sf_mma, size_t sf_mma_bytes,
-                              void* stream) {
+int moe_prepare_weight_scales(const void* sf, int E, int N, int K, int pairing, void* sf_mma,
+                              size_t sf_mma_bytes, void* stream) {
     if (!sf || !sf_mma) return MOE_ERR_INVALID_ARG;
+    if (pairing != MOE_SF_PAIRS_ADJACENT && pairing != MOE_SF_PAIRS_HALVES) return MOE_ERR_INVALID_ARG;
     const size_t need = moe_weight_scales_bytes(E, N, K);
     if (need == 0) return MOE_ERR_UNSUPPORTED;
+    if (pairing == MOE_SF_PAIRS_HALVES && (N / 2) % 128) return MOE_ERR_INVALID_ARG;
     if (sf_mma_bytes < need) return MOE_ERR_INVALID_ARG;
     int rc = device_info(nullptr);
     if (rc) return rc;
-    return cuda_status(launch_prepare_sf(static_cast<const uint8_t*>(sf), E, N, K, static_cast<uint8_t*>(sf_mma),
-                                         static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_prepare_sf(static_cast<const uint8_t*>(sf), E, N, K, pairing == MOE_SF_PAIRS_HALVES,
+                                         static_cast<uint8_t*>(sf_mma), need, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_plan(moe_plan_t* plan, const int64_t* topk_idx, const float* topk_w, int T, int k, int E, int H, int I,

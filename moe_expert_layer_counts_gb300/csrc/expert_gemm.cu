@@ -36,18 +36,19 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kBN = 256;                       // MMA N: two 128-row weight boxes
+constexpr int kBN = 256;                       // MMA N: 256 weight rows (gate|up halves for layer 1)
 constexpr int kABytes = kBlockM * kBlockK;     // 16 KB of E4M3
-constexpr int kBBoxBytes = 128 * kBlockK;      // 16 KB in smem: E2M1 unpacked to one byte per element
-constexpr int kBBoxTxBytes = 128 * kBlockK / 2; // the box's transaction count is its packed size
-constexpr int kBBytes = 2 * kBBoxBytes;
-constexpr int kSfaOff = kABytes + kBBytes;     // 512 B
-constexpr int kSfbOff = kSfaOff + kSfChunkBytes;  // 2 x 512 B
-constexpr int kStageTxBytes = kABytes + 2 * kBBoxTxBytes + 3 * kSfChunkBytes;
-constexpr int kStageStride = 51200;            // multiple of 1024 (swizzle atom alignment)
-static_assert(kSfbOff + 2 * kSfChunkBytes <= kStageStride, "stage overflow");
+constexpr int kBBytes = kBN * kBlockK;         // 32 KB in smem: E2M1 unpacked to one byte per element
+constexpr int kBTxBytes = kBN * kBlockK / 2;   // a FP4 box's transaction count is its packed size
+// A stage: A box (16 KB), the whole B tile in one request (a 3-D map for
+// layer 1 brings the gate and up rows together; a 256-row box for layer 2),
+// and two scale copies (SFA chunk, SFB chunk pair).
+constexpr int kStageSfOff = kABytes + kBBytes;   // SFA 512 B, then SFB pair 1 KB
+constexpr int kStageTxBytes = kABytes + kBTxBytes + 3 * kSfChunkBytes;
+constexpr int kStageStride = kABytes + kBBytes + 2048;  // 50 KB, a multiple of 1024
 constexpr int kBarrierBytes = 256;
 constexpr int kSmemBytes = kStages * kStageStride + kBarrierBytes + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemCol = 256;                // scale slots: 16 columns per stage
 constexpr int kThreads = 320;                  // 10 warps: TMA, MMA, 8 epilogue
@@ -60,7 +61,7 @@ struct GemmParams {
     const int* row_token;
     const float* row_weight;
     const uint8_t* sfa;     // activation scales, chunks [P_cap/128][K/128]
-    const uint8_t* sfb;     // weight scales, chunks [E][N/128][K/128]
+    const uint8_t* sfb;     // weight scales, [E][N/256 pairs][K/128][2][512]
     uint8_t* out_q;         // layer 1: E4M3 h [P_cap, I]
     uint8_t* out_sf;        // layer 1: scales of h, chunks [P_cap/128][I/128]
     uint16_t* out_bf16;     // layer 2: bf16 rows [P_cap, H]
@@ -219,36 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
-        const int nb_per_expert = p.N / 128;
-        // operand coordinates of work item w
-        struct Tile {
-            int b, row_b0, row_b1;
-            bool b1_in_range;
-            const uint8_t *sfa, *sfb0, *sfb1;
-        };
-        auto tile_of = [&](int w) {
-            Tile t;
-            t.b = w / p.n_tiles;
-            const int j = w % p.n_tiles;
-            const int e = __ldg(p.block_expert + t.b);
-            int nb0, nb1;
-            if (kLayer == 1) {
-                nb0 = j;                       // gate rows j*128..
-                nb1 = p.I / 128 + j;           // up rows I + j*128..
-            } else {
-                nb0 = 2 * j;
-                nb1 = min(2 * j + 1, nb_per_expert - 1);  // tail tile of an odd H/128: re-read, ignored
-            }
-            t.row_b0 = e * p.N + nb0 * 128;
-            t.row_b1 = e * p.N + (kLayer == 1 ? nb1 * 128 : (2 * j + 1) * 128);
-            t.b1_in_range = kLayer == 1 || 2 * j + 1 < nb_per_expert;
-            t.sfb0 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb0) * kb_count * kSfChunkBytes;
-            t.sfb1 = p.sfb + (static_cast<size_t>(e) * nb_per_expert + nb1) * kb_count * kSfChunkBytes;
-            t.sfa = p.sfa + static_cast<size_t>(t.b) * kb_count * kSfChunkBytes;
-            return t;
-        };
+        const int pairs = (p.N + 255) / 256;
         for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-            const Tile t = tile_of(w);
+            const int b = w / p.n_tiles, j = w % p.n_tiles;
+            const int e = __ldg(p.block_expert + b);
+            // layer 1: gate|up halves of expert e, rows j*128 of each (3-D map: K, row, expert-half)
+            // layer 2: rows e*H + 256*j .. +256 (2-D map)
+            const int b_y = kLayer == 1 ? j * 128 : e * p.N + j * kBN;
+            const int b_z = kLayer == 1 ? 2 * e : 0;
+            const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
+            const uint8_t* sfb = p.sfb + (static_cast<size_t>(e) * pairs + j) * kb_count * 2 * kSfChunkBytes;
             for (int kb = 0; kb < kb_count; ++kb) {
                 if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
                     ok = false;
@@ -257,13 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* st = smem + stage * kStageStride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
                 ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a, kb * kBlockK, t.b * kBlockM, full);
-                ptx::tma_load_2d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, t.row_b0, full);
-                ptx::tma_load_2d(ptx::smem_addr(st + kABytes + kBBoxBytes), &tmap_b, kb * kBlockK, t.row_b1, full);
-                ptx::bulk_load(ptx::smem_addr(st + kSfaOff), t.sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
-                ptx::bulk_load(ptx::smem_addr(st + kSfbOff), t.sfb0 + kb * kSfChunkBytes, kSfChunkBytes, full);
-                ptx::bulk_load(ptx::smem_addr(st + kSfbOff + kSfChunkBytes), t.sfb1 + kb * kSfChunkBytes,
-                               kSfChunkBytes, full);
+                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a, kb * kBlockK, b * kBlockM, full);
+                if (kLayer == 1)
+                    ptx::tma_load_3d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, b_z, full);
+                else
+                    ptx::tma_load_2d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, full);
+                ptx::bulk_load(ptx::smem_addr(st + kStageSfOff), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
+                ptx::bulk_load(ptx::smem_addr(st + kStageSfOff + kSfChunkBytes), sfb + kb * 2 * kSfChunkBytes,
+                               2 * kSfChunkBytes, full);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == kStages) {
@@ -296,9 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_fence_after();
                 const uint32_t st = ptx::smem_addr(smem + stage * kStageStride);
                 const uint32_t tsf = tmem + kSfTmemCol + 16 * stage;
-                ptx::tc_cp_32x128b_warpx4(tsf + 0, ptx::desc_sf_32x16(st + kSfaOff));
-                ptx::tc_cp_32x128b_warpx4(tsf + 4, ptx::desc_sf_32x16(st + kSfbOff));
-                ptx::tc_cp_32x128b_warpx4(tsf + 8, ptx::desc_sf_32x16(st + kSfbOff + kSfChunkBytes));
+                ptx::tc_cp_32x128b_warpx4(tsf + 0, ptx::desc_sf_32x16(st + kStageSfOff));
+                ptx::tc_cp_32x128b_warpx4(tsf + 4, ptx::desc_sf_32x16(st + kStageSfOff + kSfChunkBytes));
+                ptx::tc_cp_32x128b_warpx4(tsf + 8, ptx::desc_sf_32x16(st + kStageSfOff + 2 * kSfChunkBytes));
 #pragma unroll
                 for (int kk = 0; kk < kBlockK / 32; ++kk) {
                     const uint64_t a_desc = ptx::desc_kmajor_sw128(st + kk * 32);
@@ -411,17 +393,31 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D K-major tile map: rows x K, box 128 rows x 128 K elements, 128-byte swizzle.
+// 2-D K-major tile map: rows x K, box box_rows x 128 K elements, 128-byte swizzle.
 bool make_map(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t k_elems, uint64_t rows,
-              uint64_t row_bytes) {
+              uint64_t row_bytes, uint32_t box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {k_elems, rows};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {128, 128};
+    cuuint32_t box[2] = {128, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D FP4 map [planes][rows][K] (K-major), box 128 K x 128 rows x 2 planes:
+// one request brings the same 128 rows of two consecutive planes.
+bool make_map_3d_fp4(CUtensorMap* map, const void* base, uint64_t k_elems, uint64_t rows, uint64_t planes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {k_elems, rows, planes};
+    cuuint64_t strides[2] = {k_elems / 2, rows * (k_elems / 2)};
+    cuuint32_t box[3] = {128, 128, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -455,10 +451,13 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
         p.out_bf16 = reinterpret_cast<uint16_t*>(ws + L.l2_out);
         p.n_tiles = (L.H + kBN - 1) / kBN;
     }
-    if (!make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K) ||
-        !make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K, static_cast<uint64_t>(g.E) * g.N,
-                  g.K / 2))
-        return cudaErrorInvalidValue;
+    bool maps_ok = make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, 128);
+    if (layer == 1)  // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
+        maps_ok = maps_ok && make_map_3d_fp4(&map_b, g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
+    else
+        maps_ok = maps_ok && make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K,
+                                      static_cast<uint64_t>(g.E) * g.N, g.K / 2, kBN);
+    if (!maps_ok) return cudaErrorInvalidValue;
     static int attr_done[2][64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

@@ -50,7 +50,8 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
                          cudaStream_t s);
 cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s);
-cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, uint8_t* out, cudaStream_t s);
+cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves, uint8_t* out, size_t out_bytes,
+                              cudaStream_t s);
 
 struct GemmLaunch {
     const void* w_q;      // packed e2m1 weights [E, N, K/2]

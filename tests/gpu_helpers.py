@@ -28,8 +28,8 @@ def setup(moe, w: inputs.Workload, seed: int = 0, idx=None, tw=None):
         d["topk_idx"] = torch.as_tensor(idx, dtype=torch.int64, device="cuda").contiguous()
     if tw is not None:
         d["topk_w"] = torch.as_tensor(tw, dtype=torch.float32, device="cuda").contiguous()
-    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"])
-    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"])
+    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"], layer=1)
+    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"], layer=2)
     return d, W1, W2
 
 
