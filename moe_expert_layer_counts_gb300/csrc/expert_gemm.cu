@@ -16,15 +16,18 @@
 // Layer 2: a work item is (pool row block b, output tile j of 256 columns);
 //   epilogue rounds the fp32 accumulators to bf16 rows in pool order.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over work items):
-//   warp 0   TMA producer: A box, two B boxes, three scale chunks per stage
+// Warp roles (352 threads, one CTA per SM, persistent over work items):
+//   warp 0   TMA producer: A box, the B tile, the two scale copies per stage
 //   warp 1   tensor-memory owner and MMA issuer (one elected thread)
 //   warps 2-9 epilogue; warp w reads tensor-memory lanes 32*(w%4)..+31 and
 //            one half of the accumulator columns ((w-2)/4), so two warps
 //            share each lane quadrant
+//   warp 10  scale copies (shared memory -> tensor memory) for each stage,
+//            so that the MMA thread issues only MMAs and stage releases
 // Every wait is bounded (a global-timer deadline); on expiry the CTA records
 // an error in the workspace, waits for its own copies in flight, releases
 // tensor memory and exits.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,8 +54,10 @@ constexpr int kSmemBytes = kStages * kStageStride + kBarrierBytes + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemCol = 256;                // scale slots: 16 columns per stage
-constexpr int kThreads = 320;                  // 10 warps: TMA, MMA, 8 epilogue
+constexpr int kThreads = 320;                  // pair kernel: 10 warps (TMA, MMA, 8 epilogue)
 constexpr int kEpiWarps = 8;
+constexpr int kSingleThreads = 352;            // single-CTA kernel: 11 warps (TMA, MMA, 8 epilogue, scales)
+constexpr int kScaleWarp = 10;
 constexpr uint64_t kWaitNs = 1000000000ull;    // 1 s per wait
 
 struct GemmParams {
@@ -71,11 +76,15 @@ struct GemmParams {
     int I;                  // layer 1: intermediate size
     int H;                  // layer 2: output columns
     int* err;
+    const int* pair_block;  // 2-SM tiles: 2 * first row block + (second block present)
+    const int* n_pairs;
 };
 
 struct Shared {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t sf_ready[kStages];   // the stage's scales are in tensor memory
+    uint64_t sf_drain;
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
@@ -85,7 +94,8 @@ struct Shared {
 
 // On expiry the first CTA to give up records where: err[1] = 1 + where, with
 // where = stage (producer waiting on empty), 16 (MMA on tmem_empty),
-// 32 + stage (MMA on full), 48 (epilogue on tmem_full).
+// 32 + stage (MMA on the stage's operands and scales), 48 (epilogue on
+// tmem_full), 64 + stage (scale warp on the stage's operands).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, Shared* sh, int* err, int where) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if (ptx::mbar_wait(bar, parity, ptx::globaltimer() + kWaitNs)) return true;
@@ -178,8 +188,62 @@ __device__ __forceinline__ uint32_t requant_block(const uint32_t* gu, float wgt,
     return sbyte;
 }
 
+// Drain this warp's half of one accumulator row block from tensor memory
+// (32 lanes = 32 rows, 128 of the 256 columns) with wide loads, signal that the
+// accumulator may be overwritten (release(), once the loads have landed), and
+// pack the values as bf16 pairs: layer 1 (gate, up) of one intermediate
+// column, layer 2 two adjacent output columns.
+template <int kLayer, typename Release>
+__device__ __forceinline__ void drain_accumulator(uint32_t t_row, int half, uint32_t (&pk)[64], Release release) {
+    if (kLayer == 1) {
+        uint32_t g[64], u[64];
+        ptx::tmem_ld_32x32b_x64(t_row + 64 * half, g);
+        ptx::tmem_ld_32x32b_x64(t_row + 128 + 64 * half, u);
+        ptx::tc_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        release();
+        // gate/up rounded to bf16 (the reading of the pages' bf16 gate/up)
+#pragma unroll
+        for (int i = 0; i < 64; ++i) pk[i] = bf16x2_rn(__uint_as_float(g[i]), __uint_as_float(u[i]));
+    } else {
+        uint32_t v[128];
+        ptx::tmem_ld_32x32b_x128(t_row + 128 * half, v);
+        ptx::tc_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        release();
+#pragma unroll
+        for (int i = 0; i < 64; ++i) pk[i] = bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    }
+}
+
+// Store one pool row's share of a finished tile: layer 1 requantises 64
+// intermediate columns (two 32-blocks) to E4M3 + scales, layer 2 writes 128
+// bf16 output columns (clipped at H).
 template <int kLayer>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void store_tile_row(const GemmParams& p, int b, int j, int r, int quad, int half, int lane,
+                                               float wgt, const uint32_t (&pk)[64]) {
+    if (kLayer == 1) {
+        // intermediate columns j*128 + 64*half + [0, 64): two 32-blocks
+        uint8_t* dst = p.out_q + static_cast<size_t>(r) * p.I + j * 128 + 64 * half;
+        const uint32_t s0 = requant_block(pk, wgt, dst);
+        const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32);
+        const size_t chunk = static_cast<size_t>(b) * (p.I / 128) + j;
+        *reinterpret_cast<uint16_t*>(p.out_sf + chunk * kSfChunkBytes + 16 * lane + 4 * quad + 2 * half) =
+            static_cast<uint16_t>(s0 | (s1 << 8));
+    } else {
+        const int col0 = j * kBN + 128 * half;
+        const int ncol = p.H - col0;
+        uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + static_cast<size_t>(r) * p.H + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (8 * i < ncol) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+}
+
+template <int kLayer>
+__global__ void __launch_bounds__(kSingleThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const GemmParams p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
@@ -196,7 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(&sh->full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh->empty[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh->sf_ready[s]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&sh->sf_drain), 1);
         ptx::mbar_init(ptx::smem_addr(&sh->tmem_full), 1);
         ptx::mbar_init(ptx::smem_addr(&sh->tmem_empty), kEpiWarps);
         ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
@@ -263,7 +329,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
+        // The issue rate of one thread bounds the MMA rate (each tcgen05
+        // instruction takes tens of cycles to issue), so this thread issues
+        // only the MMAs and the stage release; the scale copies come from the
+        // scale warp, and everything that does not change with the k-block is
+        // computed once.  A stage's shared-memory descriptors are those of
+        // stage 0 plus the stage offset in 16-byte units (the start-address
+        // field); a 32-wide K step adds 2.
         constexpr uint32_t idesc = ptx::idesc_e4m3_e2m1(kBlockM, kBN);
+        const uint32_t st0 = ptx::smem_addr(smem);
+        const uint64_t a_desc0 = ptx::desc_kmajor_sw128(st0);
+        const uint64_t b_desc0 = ptx::desc_kmajor_sw128(st0 + kABytes);
+        const uint32_t ready0 = ptx::smem_addr(&sh->sf_ready[0]);
+        const uint32_t empty0 = ptx::smem_addr(&sh->empty[0]);
+        const uint32_t tsf0 = tmem + kSfTmemCol;
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true;
@@ -271,24 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->tmem_empty), acc_phase ^ 1, sh, p.err, 16)) break;
             ptx::tc_fence_after();
             for (int kb = 0; kb < kb_count; ++kb) {
-                if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->full[stage]), phase, sh, p.err, 32 + stage)) {
+                // the stage's operands have landed and its scales are in tensor memory
+                if (!wait_or_abort(ready0 + 8 * stage, phase, sh, p.err, 32 + stage)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t st = ptx::smem_addr(smem + stage * kStageStride);
-                const uint32_t tsf = tmem + kSfTmemCol + 16 * stage;
-                ptx::tc_cp_32x128b_warpx4(tsf + 0, ptx::desc_sf_32x16(st + kStageSfOff));
-                ptx::tc_cp_32x128b_warpx4(tsf + 4, ptx::desc_sf_32x16(st + kStageSfOff + kSfChunkBytes));
-                ptx::tc_cp_32x128b_warpx4(tsf + 8, ptx::desc_sf_32x16(st + kStageSfOff + 2 * kSfChunkBytes));
+                const uint64_t so = static_cast<uint64_t>(stage * (kStageStride >> 4));
+                const uint32_t tsf = tsf0 + 16 * stage;
 #pragma unroll
-                for (int kk = 0; kk < kBlockK / 32; ++kk) {
-                    const uint64_t a_desc = ptx::desc_kmajor_sw128(st + kk * 32);
-                    const uint64_t b_desc = ptx::desc_kmajor_sw128(st + kABytes + kk * 32);
-                    ptx::mma_mxf8f6f4(tmem, a_desc, b_desc, ptx::idesc_with_sf_id(idesc, kk), tsf + 0, tsf + 4,
-                                      (kb | kk) != 0);
-                }
-                ptx::tc_commit(ptx::smem_addr(&sh->empty[stage]));
+                for (int kk = 0; kk < kBlockK / 32; ++kk)
+                    ptx::mma_mxf8f6f4(tmem, a_desc0 + so + 2 * kk, b_desc0 + so + 2 * kk,
+                                      ptx::idesc_with_sf_id(idesc, kk), tsf + 0, tsf + 4, (kb | kk) != 0);
+                ptx::tc_commit(empty0 + 8 * stage);
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1;
@@ -301,7 +375,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all tensor-core work of this CTA done before tensor memory is freed
         ptx::tc_commit(ptx::smem_addr(&sh->drain));
         ptx::mbar_wait(ptx::smem_addr(&sh->drain), 0, ptx::globaltimer() + kWaitNs);
-    } else if (warp >= 2) {
+    } else if (warp == kScaleWarp && lane == 0) {
+        // ------------------------------------------------ scale copies
+        // Per k-block, once the stage has landed: the A scale chunk and the
+        // B scale pair into the stage's tensor-memory slot, then signal the
+        // MMA thread.  The slot is free by then: the stage was refilled only
+        // after the MMAs that last read the slot had completed.
+        const uint64_t sf_desc0 = ptx::desc_sf_32x16(ptx::smem_addr(smem) + kStageSfOff);
+        const uint32_t full0 = ptx::smem_addr(&sh->full[0]);
+        const uint32_t ready0 = ptx::smem_addr(&sh->sf_ready[0]);
+        const uint32_t tsf0 = tmem + kSfTmemCol;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+            for (int kb = 0; kb < kb_count; ++kb) {
+                if (!wait_or_abort(full0 + 8 * stage, phase, sh, p.err, 64 + stage)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint64_t so = static_cast<uint64_t>(stage * (kStageStride >> 4));
+                const uint32_t tsf = tsf0 + 16 * stage;
+                ptx::tc_cp_32x128b_warpx4(tsf + 0, sf_desc0 + so);
+                ptx::tc_cp_32x128b_warpx4(tsf + 4, sf_desc0 + so + (kSfChunkBytes >> 4));
+                ptx::tc_cp_32x128b_warpx4(tsf + 8, sf_desc0 + so + (2 * kSfChunkBytes >> 4));
+                ptx::tc_commit(ready0 + 8 * stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        // its copies complete before tensor memory is freed
+        ptx::tc_commit(ptx::smem_addr(&sh->sf_drain));
+        ptx::mbar_wait(ptx::smem_addr(&sh->sf_drain), 0, ptx::globaltimer() + kWaitNs);
+    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
         // ------------------------------------------------ epilogue
         const int quad = warp & 3;
         const int half = (warp - 2) / 4;                // which half of the accumulator columns
@@ -317,49 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool go = !aborted(sh) && wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p.err, 48);
             if (!__all_sync(0xffffffffu, go)) break;
             ptx::tc_fence_after();
-            // Drain this warp's half of the accumulator row into registers with
-            // wide loads and release tensor memory at once, so the next tile's
-            // MMAs start while this epilogue converts and stores.
             uint32_t pk[64];
-            if (kLayer == 1) {
-                uint32_t g[64], u[64];
-                ptx::tmem_ld_32x32b_x64(t_row + 64 * half, g);
-                ptx::tmem_ld_32x32b_x64(t_row + 128 + 64 * half, u);
-                ptx::tc_wait_ld();
-                ptx::tc_fence_before();
-                __syncwarp();
+            drain_accumulator<kLayer>(t_row, half, pk, [&] {
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
-                // gate/up rounded to bf16 (the reading of the pages' bf16 gate/up)
-#pragma unroll
-                for (int i = 0; i < 64; ++i) pk[i] = bf16x2_rn(__uint_as_float(g[i]), __uint_as_float(u[i]));
-            } else {
-                uint32_t v[128];
-                ptx::tmem_ld_32x32b_x128(t_row + 128 * half, v);
-                ptx::tc_wait_ld();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
-#pragma unroll
-                for (int i = 0; i < 64; ++i) pk[i] = bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            }
-            if (tok >= 0) {
-                if (kLayer == 1) {
-                    // intermediate columns j*128 + 64*half + [0, 64): two 32-blocks
-                    uint8_t* dst = p.out_q + static_cast<size_t>(r) * p.I + j * 128 + 64 * half;
-                    const uint32_t s0 = requant_block(pk, wgt, dst);
-                    const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32);
-                    const size_t chunk = static_cast<size_t>(b) * (p.I / 128) + j;
-                    *reinterpret_cast<uint16_t*>(p.out_sf + chunk * kSfChunkBytes + 16 * lane + 4 * quad + 2 * half) =
-                        static_cast<uint16_t>(s0 | (s1 << 8));
-                } else {
-                    const int col0 = j * kBN + 128 * half;
-                    const int ncol = p.H - col0;
-                    uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + static_cast<size_t>(r) * p.H + col0);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (8 * i < ncol) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-            }
+            });
+            if (tok >= 0) store_tile_row<kLayer>(p, b, j, r, quad, half, lane, wgt, pk);
             acc_phase ^= 1;
         }
     }
@@ -369,6 +440,242 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
+#else
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kDevErrTimeout);
+#endif
+}
+
+// ---------------------------------------------------------------------------
+// 2-SM variant: a cluster of two CTAs on one TPC computes a 256 x 256 tile with
+// the pair MMA (cta_group::2).  A work item is (pair of row blocks of one
+// expert, N tile j); CTA r of the pair holds row block (first + r) of A and
+// weight rows [128 r, 128 r + 128) of the 256-row B tile, so each SM stages
+// and reads half of B per k-block instead of all of it.  Each CTA also stages
+// its own A scale chunk and the whole B scale pair.  Every TMA load of both
+// CTAs completes on the even CTA's `full` barrier; its single MMA thread
+// issues the scale copies and MMAs for the pair and signals both CTAs'
+// `empty` / `tmem_full` barriers; the epilogue warps of both CTAs release the
+// accumulator on the even CTA's `tmem_empty` barrier.  If an expert has an odd
+// number of row blocks, its last pair has no second block: the odd CTA loads
+// no A for it and its accumulator rows are discarded.
+constexpr int kPStages = 6;
+constexpr int kPBRows = kBN / 2;                           // B rows held by each CTA
+constexpr int kPBBytes = kPBRows * kBlockK;                // 16 KB unpacked
+constexpr int kPBTxBytes = kPBRows * kBlockK / 2;          // 8 KB packed
+constexpr int kPSfaOff = kABytes + kPBBytes;               // SFA chunk, then the SFB pair
+constexpr int kPSfbOff = kPSfaOff + kSfChunkBytes;
+constexpr int kPStageStride = kABytes + kPBBytes + 2048;   // 34 KB, a multiple of 1024
+constexpr int kPStageTxBytes = kABytes + kPBTxBytes + 3 * kSfChunkBytes;
+constexpr int kPSmemBytes = kPStages * kPStageStride + kBarrierBytes + 1024;
+static_assert(kPSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSfTmemCol + 16 * kPStages <= kTmemCols, "tensor memory budget");
+
+struct PairShared {
+    uint64_t full[kPStages];
+    uint64_t empty[kPStages];
+    uint64_t tmem_full;
+    uint64_t tmem_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(PairShared) <= kBarrierBytes, "barrier area");
+
+__device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, PairShared* sh, int* err,
+                                                   int where) {
+    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if (ptx::mbar_wait_cluster(bar, parity, ptx::globaltimer() + kWaitNs)) return true;
+    atomicOr(err, kDevErrTimeout);
+    atomicCAS(err + 1, 0, 1 + where);
+    *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+    return false;
+}
+__device__ __forceinline__ bool pair_aborted(PairShared* sh) {
+    return *reinterpret_cast<volatile int*>(&sh->abort) != 0;
+}
+
+template <int kLayer>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                            const GemmParams p) {
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairShared* sh = reinterpret_cast<PairShared*>(smem + kPStages * kPStageStride);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cluster = static_cast<int>(ptx::cluster_id_x());
+    const int n_clusters = static_cast<int>(ptx::num_clusters_x());
+
+    const int n_work = *p.n_pairs * p.n_tiles;
+    if (cluster >= n_work) return;  // uniform for both CTAs of the pair
+    const int kb_count = p.K / kBlockK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sh->full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh->empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&sh->tmem_full), 1);
+        ptx::mbar_init(ptx::smem_addr(&sh->tmem_empty), 2 * kEpiWarps);
+        ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
+        sh->abort = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&tmap_a);
+        ptx::prefetch_tensormap(&tmap_b);
+        ptx::prefetch_tensormap(&tmap_sfa);
+        ptx::prefetch_tensormap(&tmap_sfb);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr(&sh->tmem_base), kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // both CTAs' barriers initialised, tensor memory allocated
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&sh->tmem_base);
+    const int pairs = (p.N + 255) / 256;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        bool ok = true;
+        for (int w = cluster; w < n_work && ok; w += n_clusters) {
+            const int pe = __ldg(p.pair_block + w / p.n_tiles), j = w % p.n_tiles;
+            const int first = pe >> 1;
+            const bool second = (pe & 1) != 0;
+            const bool own_a = rank == 0 || second;
+            const int b = first + static_cast<int>(rank);
+            const int e = __ldg(p.block_expert + first);
+            // layer 1: CTA 0 the gate rows j*128.., CTA 1 the up rows I + j*128..
+            // layer 2: rows j*256 + 128*rank of expert e's H rows
+            const int b_y = kLayer == 1 ? e * p.N + static_cast<int>(rank) * p.I + j * 128
+                                        : e * p.N + j * kBN + static_cast<int>(rank) * kPBRows;
+            const int sfa_y = 2 * b * kb_count;
+            const int sfb_y = 4 * (e * pairs + j) * kb_count;
+            const uint32_t tx = kPStageTxBytes + (second ? kPStageTxBytes : kPStageTxBytes - kABytes - kSfChunkBytes);
+            for (int kb = 0; kb < kb_count; ++kb) {
+                if (pair_aborted(sh) ||
+                    !pair_wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* st = smem + stage * kPStageStride;
+                const uint32_t full = ptx::map_to_rank(ptx::smem_addr(&sh->full[stage]), 0);  // the even CTA's
+                if (rank == 0) ptx::mbar_arrive_expect_tx(ptx::smem_addr(&sh->full[stage]), tx);
+                if (own_a) {
+                    ptx::tma_load_2d_pair(ptx::smem_addr(st), &tmap_a, kb * kBlockK, b * kBlockM, full);
+                    ptx::tma_load_2d_pair(ptx::smem_addr(st + kPSfaOff), &tmap_sfa, 0, sfa_y + 2 * kb, full);
+                }
+                ptx::tma_load_2d_pair(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, full);
+                ptx::tma_load_2d_pair(ptx::smem_addr(st + kPSfbOff), &tmap_sfb, 0, sfb_y + 4 * kb, full);
+                issued_mask |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            // let the copies in flight land before the CTA may exit: the even
+            // CTA waits on its barriers, the odd one (whose copies complete
+            // there) gives them a fixed time
+            if (rank == 0) {
+                for (int s = 0; s < kPStages; ++s)
+                    if (issued_mask & (1u << s))
+                        ptx::mbar_wait_cluster(ptx::smem_addr(&sh->full[s]), (issued_parity >> s) & 1u,
+                                               ptx::globaltimer() + kWaitNs);
+            } else {
+                const uint64_t until = ptx::globaltimer() + 1000000ull;
+                while (ptx::globaltimer() < until) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ------------------------------------------------ MMA issuer (even CTA, for the pair)
+        constexpr uint32_t idesc = ptx::idesc_e4m3_e2m1(2 * kBlockM, kBN);
+        const uint32_t tfull_addr = ptx::smem_addr(&sh->tmem_full);
+        int stage = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        bool ok = true;
+        for (int w = cluster; w < n_work && ok; w += n_clusters) {
+            if (pair_aborted(sh) ||
+                !pair_wait_or_abort(ptx::smem_addr(&sh->tmem_empty), acc_phase ^ 1, sh, p.err, 16))
+                break;
+            ptx::tc_fence_after();
+            for (int kb = 0; kb < kb_count; ++kb) {
+                if (pair_aborted(sh) ||
+                    !pair_wait_or_abort(ptx::smem_addr(&sh->full[stage]), phase, sh, p.err, 32 + stage)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t st = ptx::smem_addr(smem + stage * kPStageStride);
+                const uint32_t tsf = tmem + kSfTmemCol + 16 * stage;
+                ptx::tc_cp_32x128b_warpx4_pair(tsf + 0, ptx::desc_sf_32x16(st + kPSfaOff));
+                ptx::tc_cp_32x128b_warpx4_pair(tsf + 4, ptx::desc_sf_32x16(st + kPSfbOff));
+                ptx::tc_cp_32x128b_warpx4_pair(tsf + 8, ptx::desc_sf_32x16(st + kPSfbOff + kSfChunkBytes));
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / 32; ++kk) {
+                    const uint64_t a_desc = ptx::desc_kmajor_sw128(st + kk * 32);
+                    const uint64_t b_desc = ptx::desc_kmajor_sw128(st + kABytes + kk * 32);
+                    ptx::mma_mxf8f6f4_pair(tmem, a_desc, b_desc, ptx::idesc_with_sf_id(idesc, kk), tsf + 0, tsf + 4,
+                                           (kb | kk) != 0);
+                }
+                ptx::tc_commit_pair(ptx::map_to_rank(ptx::smem_addr(&sh->empty[stage]), 0));
+                ptx::tc_commit_pair(ptx::map_to_rank(ptx::smem_addr(&sh->empty[stage]), 1));
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            ptx::tc_commit_pair(ptx::map_to_rank(tfull_addr, 0));
+            ptx::tc_commit_pair(ptx::map_to_rank(tfull_addr, 1));
+            acc_phase ^= 1;
+        }
+        // all tensor-core work of the pair done before tensor memory is freed
+        ptx::tc_commit_pair(ptx::map_to_rank(ptx::smem_addr(&sh->drain), 0));
+        ptx::mbar_wait_cluster(ptx::smem_addr(&sh->drain), 0, ptx::globaltimer() + kWaitNs);
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int quad = warp & 3;
+        const int half = (warp - 2) / 4;
+        const int m = quad * 32 + lane;
+        const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+        const uint32_t release_addr = ptx::map_to_rank(ptx::smem_addr(&sh->tmem_empty), 0);
+        uint32_t acc_phase = 0;
+        for (int w = cluster; w < n_work; w += n_clusters) {
+            const int pe = __ldg(p.pair_block + w / p.n_tiles), j = w % p.n_tiles;
+            const bool own_rows = rank == 0 || (pe & 1) != 0;
+            const int b = (pe >> 1) + static_cast<int>(rank);
+            const int r = b * kBlockM + m;
+            const int tok = own_rows ? __ldg(p.row_token + r) : -1;
+            const float wgt = own_rows ? __ldg(p.row_weight + r) : 0.0f;
+            const bool go =
+                !pair_aborted(sh) && pair_wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p.err, 48);
+            if (!__all_sync(0xffffffffu, go)) break;
+            ptx::tc_fence_after();
+            uint32_t pk[64];
+            drain_accumulator<kLayer>(t_row, half, pk, [&] {
+                if (lane == 0) ptx::mbar_arrive_cluster(release_addr);
+            });
+            if (tok >= 0) store_tile_row<kLayer>(p, b, j, r, quad, half, lane, wgt, pk);
+            acc_phase ^= 1;
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::cluster_sync();  // the pair's MMAs are complete (the even CTA waited on `drain`)
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    }
+    ptx::cluster_sync();
 #else
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kDevErrTimeout);
 #endif
@@ -421,6 +728,94 @@ bool make_map_3d_fp4(CUtensorMap* map, const void* base, uint64_t k_elems, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale chunks seen by TMA as rows of 256 bytes: a box of `box_rows` rows
+// brings box_rows / 2 consecutive 512-byte chunks.
+bool make_sf_map(CUtensorMap* map, const void* base, uint64_t bytes, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {256, bytes / 256};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+namespace {
+
+// Opt a kernel into its dynamic shared memory once per device.
+template <typename Kernel>
+cudaError_t smem_attr_once(Kernel kernel, int slot, int bytes) {
+    static int done[4][64] = {};
+    int dev = 0;
+    cudaError_t st = cudaGetDevice(&dev);
+    if (st != cudaSuccess) return st;
+    if (dev < 64 && done[slot][dev]) return cudaSuccess;
+    st = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (st == cudaSuccess && dev < 64) done[slot][dev] = 1;
+    return st;
+}
+
+}  // namespace
+
+namespace {
+
+// One CTA per SM, 128-row tiles: B arrives as one request per stage (a 3-D
+// map brings the gate and up rows for layer 1, a 256-row box for layer 2).
+cudaError_t launch_single(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
+                          int num_sms, cudaStream_t s) {
+    CUtensorMap map_a, map_b;
+    bool maps_ok = make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, kBlockM);
+    if (layer == 1)  // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
+        maps_ok = maps_ok && make_map_3d_fp4(&map_b, g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
+    else
+        maps_ok = maps_ok && make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K,
+                                      static_cast<uint64_t>(g.E) * g.N, g.K / 2, kBN);
+    if (!maps_ok) return cudaErrorInvalidValue;
+    cudaError_t st;
+    if (layer == 1) {
+        if ((st = smem_attr_once(expert_gemm_kernel<1>, 2, kSmemBytes)) != cudaSuccess) return st;
+        expert_gemm_kernel<1><<<num_sms, kSingleThreads, kSmemBytes, s>>>(map_a, map_b, p);
+    } else {
+        if ((st = smem_attr_once(expert_gemm_kernel<2>, 3, kSmemBytes)) != cudaSuccess) return st;
+        expert_gemm_kernel<2><<<num_sms, kSingleThreads, kSmemBytes, s>>>(map_a, map_b, p);
+    }
+    return cudaGetLastError();
+}
+
+// CTA pairs (2-SM MMA), 256-row tiles over the pair table.
+cudaError_t launch_pair(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
+                        int num_sms, cudaStream_t s) {
+    const uint64_t kb_count = static_cast<uint64_t>(g.K) / kBlockK;
+    const uint64_t sfa_bytes = static_cast<uint64_t>(L.p_cap / kBlockM) * kb_count * kSfChunkBytes;
+    const uint64_t sfb_bytes = static_cast<uint64_t>(g.E) * ((g.N + 255) / 256) * kb_count * 2 * kSfChunkBytes;
+    // A: pool rows, 128-row boxes; B: all experts' weight rows [E*N, K],
+    // 128-row boxes (one half of the 256-row tile per CTA); scales as
+    // 256-byte rows (an SFA chunk = 2 rows, an SFB chunk pair = 4 rows).
+    CUtensorMap map_a, map_b, map_sfa, map_sfb;
+    const bool maps_ok =
+        make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, kBlockM) &&
+        make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K, static_cast<uint64_t>(g.E) * g.N, g.K / 2,
+                 kPBRows) &&
+        make_sf_map(&map_sfa, p.sfa, sfa_bytes, 2) && make_sf_map(&map_sfb, p.sfb, sfb_bytes, 4);
+    if (!maps_ok) return cudaErrorInvalidValue;
+    const int grid = std::max(2, num_sms / 2 * 2);
+    cudaError_t st;
+    if (layer == 1) {
+        if ((st = smem_attr_once(expert_gemm_pair_kernel<1>, 0, kPSmemBytes)) != cudaSuccess) return st;
+        expert_gemm_pair_kernel<1><<<grid, kThreads, kPSmemBytes, s>>>(map_a, map_b, map_sfa, map_sfb, p);
+    } else {
+        if ((st = smem_attr_once(expert_gemm_pair_kernel<2>, 1, kPSmemBytes)) != cudaSuccess) return st;
+        expert_gemm_pair_kernel<2><<<grid, kThreads, kPSmemBytes, s>>>(map_a, map_b, map_sfa, map_sfb, p);
+    }
+    return cudaGetLastError();
+}
+
+constexpr bool kUsePair = false;
+
 }  // namespace
 
 cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,
@@ -429,6 +824,8 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     GemmParams p{};
     p.n_blocks = reinterpret_cast<const int*>(ws + L.n_blocks);
     p.block_expert = reinterpret_cast<const int*>(ws + L.block_expert);
+    p.pair_block = reinterpret_cast<const int*>(ws + L.pair_block);
+    p.n_pairs = reinterpret_cast<const int*>(ws + L.n_pairs);
     p.row_token = reinterpret_cast<const int*>(ws + L.row_token);
     p.row_weight = reinterpret_cast<const float*>(ws + L.row_weight);
     p.sfb = static_cast<const uint8_t*>(g.w_sf);
@@ -437,7 +834,6 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     p.I = L.I;
     p.H = L.H;
     p.err = reinterpret_cast<int*>(ws + L.err);
-    CUtensorMap map_a, map_b;
     const void* a_base;
     if (layer == 1) {
         a_base = ws + L.pool_q;
@@ -451,33 +847,8 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
         p.out_bf16 = reinterpret_cast<uint16_t*>(ws + L.l2_out);
         p.n_tiles = (L.H + kBN - 1) / kBN;
     }
-    bool maps_ok = make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, 128);
-    if (layer == 1)  // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
-        maps_ok = maps_ok && make_map_3d_fp4(&map_b, g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
-    else
-        maps_ok = maps_ok && make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K,
-                                      static_cast<uint64_t>(g.E) * g.N, g.K / 2, kBN);
-    if (!maps_ok) return cudaErrorInvalidValue;
-    static int attr_done[2][64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaError_t st;
-    if (layer == 1) {
-        if (dev < 64 && !attr_done[0][dev]) {
-            st = cudaFuncSetAttribute(expert_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            if (st != cudaSuccess) return st;
-            attr_done[0][dev] = 1;
-        }
-        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_b, p);
-    } else {
-        if (dev < 64 && !attr_done[1][dev]) {
-            st = cudaFuncSetAttribute(expert_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            if (st != cudaSuccess) return st;
-            attr_done[1][dev] = 1;
-        }
-        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_b, p);
-    }
-    return cudaGetLastError();
+    return kUsePair ? launch_pair(layer, L, g, a_base, p, num_sms, s)
+                    : launch_single(layer, L, g, a_base, p, num_sms, s);
 }
 
 }  // namespace moe
