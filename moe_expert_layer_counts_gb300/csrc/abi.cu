@@ -114,14 +114,12 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
     };
     L->err = take(2 * sizeof(int));
     L->n_blocks = take(sizeof(int));
-    L->n_pairs = take(sizeof(int));
     L->count = take(sizeof(int) * E);
     L->off = take(sizeof(int) * (E + 1));
     L->poff = take(sizeof(int) * (E + 1));
     L->hist = take(sizeof(int) * static_cast<size_t>(chunks) * E);
     L->chunk_base = take(sizeof(int) * static_cast<size_t>(chunks) * E);
     L->block_expert = take(sizeof(int) * static_cast<size_t>(cap / kBlockM));
-    L->pair_block = take(sizeof(int) * static_cast<size_t>(cap / kBlockM));
     L->slot_of = take(sizeof(int) * static_cast<size_t>(std::max<int64_t>(n, 1)));
     L->row_token = take(sizeof(int) * static_cast<size_t>(cap));
     L->row_topk = take(sizeof(int) * static_cast<size_t>(cap));
@@ -291,8 +289,6 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
         case MOE_EXPORT_L2_OUT: *offset = L.l2_out; *bytes = cap * ps->H * 2; break;
         case MOE_EXPORT_ERROR: *offset = L.err; *bytes = 8; break;
         case MOE_EXPORT_POOL_ROWS: *offset = 0; *bytes = cap; break;
-        case MOE_EXPORT_PAIR_BLOCK: *offset = L.pair_block; *bytes = 4 * (cap / kBlockM); break;
-        case MOE_EXPORT_NUM_PAIRS: *offset = L.n_pairs; *bytes = 4; break;
         default: return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;

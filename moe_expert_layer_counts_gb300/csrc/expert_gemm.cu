@@ -27,7 +27,6 @@
 // Every wait is bounded (a global-timer deadline); on expiry the CTA records
 // an error in the workspace, waits for its own copies in flight, releases
 // tensor memory and exits.
-#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,9 +53,8 @@ constexpr int kSmemBytes = kStages * kStageStride + kBarrierBytes + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemCol = 256;                // scale slots: 16 columns per stage
-constexpr int kThreads = 320;                  // pair kernel: 10 warps (TMA, MMA, 8 epilogue)
+constexpr int kThreads = 352;                  // 11 warps: TMA, MMA, 8 epilogue, scale copies
 constexpr int kEpiWarps = 8;
-constexpr int kSingleThreads = 352;            // single-CTA kernel: 11 warps (TMA, MMA, 8 epilogue, scales)
 constexpr int kScaleWarp = 10;
 constexpr uint64_t kWaitNs = 1000000000ull;    // 1 s per wait
 
@@ -76,8 +74,6 @@ struct GemmParams {
     int I;                  // layer 1: intermediate size
     int H;                  // layer 2: output columns
     int* err;
-    const int* pair_block;  // 2-SM tiles: 2 * first row block + (second block present)
-    const int* n_pairs;
 };
 
 struct Shared {
@@ -243,7 +239,7 @@ __device__ __forceinline__ void store_tile_row(const GemmParams& p, int b, int j
 }
 
 template <int kLayer>
-__global__ void __launch_bounds__(kSingleThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const GemmParams p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
@@ -378,9 +374,12 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
     } else if (warp == kScaleWarp && lane == 0) {
         // ------------------------------------------------ scale copies
         // Per k-block, once the stage has landed: the A scale chunk and the
-        // B scale pair into the stage's tensor-memory slot, then signal the
-        // MMA thread.  The slot is free by then: the stage was refilled only
-        // after the MMAs that last read the slot had completed.
+        // B scale pair into the stage's tensor-memory slot, then an ordered
+        // hand-off to the MMA thread (fence before the arrive here, fence
+        // after the wait there), so the MMAs queue behind the copies without
+        // waiting for them to complete.  The slot is free by then: the stage
+        // was refilled only after the MMAs that last read the slot had
+        // completed.
         const uint64_t sf_desc0 = ptx::desc_sf_32x16(ptx::smem_addr(smem) + kStageSfOff);
         const uint32_t full0 = ptx::smem_addr(&sh->full[0]);
         const uint32_t ready0 = ptx::smem_addr(&sh->sf_ready[0]);
@@ -400,7 +399,10 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
                 ptx::tc_cp_32x128b_warpx4(tsf + 0, sf_desc0 + so);
                 ptx::tc_cp_32x128b_warpx4(tsf + 4, sf_desc0 + so + (kSfChunkBytes >> 4));
                 ptx::tc_cp_32x128b_warpx4(tsf + 8, sf_desc0 + so + (2 * kSfChunkBytes >> 4));
-                ptx::tc_commit(ready0 + 8 * stage);
+                // ordered hand-off: the MMAs the MMA thread issues after it has
+                // seen this arrive (and fenced) execute after these copies
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ready0 + 8 * stage);
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1;
@@ -440,242 +442,6 @@ __global__ void __launch_bounds__(kSingleThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
-#else
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kDevErrTimeout);
-#endif
-}
-
-// ---------------------------------------------------------------------------
-// 2-SM variant: a cluster of two CTAs on one TPC computes a 256 x 256 tile with
-// the pair MMA (cta_group::2).  A work item is (pair of row blocks of one
-// expert, N tile j); CTA r of the pair holds row block (first + r) of A and
-// weight rows [128 r, 128 r + 128) of the 256-row B tile, so each SM stages
-// and reads half of B per k-block instead of all of it.  Each CTA also stages
-// its own A scale chunk and the whole B scale pair.  Every TMA load of both
-// CTAs completes on the even CTA's `full` barrier; its single MMA thread
-// issues the scale copies and MMAs for the pair and signals both CTAs'
-// `empty` / `tmem_full` barriers; the epilogue warps of both CTAs release the
-// accumulator on the even CTA's `tmem_empty` barrier.  If an expert has an odd
-// number of row blocks, its last pair has no second block: the odd CTA loads
-// no A for it and its accumulator rows are discarded.
-constexpr int kPStages = 6;
-constexpr int kPBRows = kBN / 2;                           // B rows held by each CTA
-constexpr int kPBBytes = kPBRows * kBlockK;                // 16 KB unpacked
-constexpr int kPBTxBytes = kPBRows * kBlockK / 2;          // 8 KB packed
-constexpr int kPSfaOff = kABytes + kPBBytes;               // SFA chunk, then the SFB pair
-constexpr int kPSfbOff = kPSfaOff + kSfChunkBytes;
-constexpr int kPStageStride = kABytes + kPBBytes + 2048;   // 34 KB, a multiple of 1024
-constexpr int kPStageTxBytes = kABytes + kPBTxBytes + 3 * kSfChunkBytes;
-constexpr int kPSmemBytes = kPStages * kPStageStride + kBarrierBytes + 1024;
-static_assert(kPSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kSfTmemCol + 16 * kPStages <= kTmemCols, "tensor memory budget");
-
-struct PairShared {
-    uint64_t full[kPStages];
-    uint64_t empty[kPStages];
-    uint64_t tmem_full;
-    uint64_t tmem_empty;
-    uint64_t drain;
-    uint32_t tmem_base;
-    int abort;
-};
-static_assert(sizeof(PairShared) <= kBarrierBytes, "barrier area");
-
-__device__ __forceinline__ bool pair_wait_or_abort(uint32_t bar, uint32_t parity, PairShared* sh, int* err,
-                                                   int where) {
-    if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
-    if (ptx::mbar_wait_cluster(bar, parity, ptx::globaltimer() + kWaitNs)) return true;
-    atomicOr(err, kDevErrTimeout);
-    atomicCAS(err + 1, 0, 1 + where);
-    *reinterpret_cast<volatile int*>(&sh->abort) = 1;
-    return false;
-}
-__device__ __forceinline__ bool pair_aborted(PairShared* sh) {
-    return *reinterpret_cast<volatile int*>(&sh->abort) != 0;
-}
-
-template <int kLayer>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                            const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-                            const GemmParams p) {
-#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    PairShared* sh = reinterpret_cast<PairShared*>(smem + kPStages * kPStageStride);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();
-    const int cluster = static_cast<int>(ptx::cluster_id_x());
-    const int n_clusters = static_cast<int>(ptx::num_clusters_x());
-
-    const int n_work = *p.n_pairs * p.n_tiles;
-    if (cluster >= n_work) return;  // uniform for both CTAs of the pair
-    const int kb_count = p.K / kBlockK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kPStages; ++s) {
-            ptx::mbar_init(ptx::smem_addr(&sh->full[s]), 1);
-            ptx::mbar_init(ptx::smem_addr(&sh->empty[s]), 1);
-        }
-        ptx::mbar_init(ptx::smem_addr(&sh->tmem_full), 1);
-        ptx::mbar_init(ptx::smem_addr(&sh->tmem_empty), 2 * kEpiWarps);
-        ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
-        sh->abort = 0;
-        ptx::fence_mbar_init();
-        ptx::prefetch_tensormap(&tmap_a);
-        ptx::prefetch_tensormap(&tmap_b);
-        ptx::prefetch_tensormap(&tmap_sfa);
-        ptx::prefetch_tensormap(&tmap_sfb);
-    }
-    if (warp == 1) {
-        ptx::tmem_alloc_pair(ptx::smem_addr(&sh->tmem_base), kTmemCols);
-        ptx::tmem_relinquish_pair();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::cluster_sync();  // both CTAs' barriers initialised, tensor memory allocated
-    ptx::tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&sh->tmem_base);
-    const int pairs = (p.N + 255) / 256;
-
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ TMA producer (both CTAs)
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t issued_mask = 0, issued_parity = 0;
-        bool ok = true;
-        for (int w = cluster; w < n_work && ok; w += n_clusters) {
-            const int pe = __ldg(p.pair_block + w / p.n_tiles), j = w % p.n_tiles;
-            const int first = pe >> 1;
-            const bool second = (pe & 1) != 0;
-            const bool own_a = rank == 0 || second;
-            const int b = first + static_cast<int>(rank);
-            const int e = __ldg(p.block_expert + first);
-            // layer 1: CTA 0 the gate rows j*128.., CTA 1 the up rows I + j*128..
-            // layer 2: rows j*256 + 128*rank of expert e's H rows
-            const int b_y = kLayer == 1 ? e * p.N + static_cast<int>(rank) * p.I + j * 128
-                                        : e * p.N + j * kBN + static_cast<int>(rank) * kPBRows;
-            const int sfa_y = 2 * b * kb_count;
-            const int sfb_y = 4 * (e * pairs + j) * kb_count;
-            const uint32_t tx = kPStageTxBytes + (second ? kPStageTxBytes : kPStageTxBytes - kABytes - kSfChunkBytes);
-            for (int kb = 0; kb < kb_count; ++kb) {
-                if (pair_aborted(sh) ||
-                    !pair_wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* st = smem + stage * kPStageStride;
-                const uint32_t full = ptx::map_to_rank(ptx::smem_addr(&sh->full[stage]), 0);  // the even CTA's
-                if (rank == 0) ptx::mbar_arrive_expect_tx(ptx::smem_addr(&sh->full[stage]), tx);
-                if (own_a) {
-                    ptx::tma_load_2d_pair(ptx::smem_addr(st), &tmap_a, kb * kBlockK, b * kBlockM, full);
-                    ptx::tma_load_2d_pair(ptx::smem_addr(st + kPSfaOff), &tmap_sfa, 0, sfa_y + 2 * kb, full);
-                }
-                ptx::tma_load_2d_pair(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, full);
-                ptx::tma_load_2d_pair(ptx::smem_addr(st + kPSfbOff), &tmap_sfb, 0, sfb_y + 4 * kb, full);
-                issued_mask |= 1u << stage;
-                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kPStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-        }
-        if (!ok) {
-            // let the copies in flight land before the CTA may exit: the even
-            // CTA waits on its barriers, the odd one (whose copies complete
-            // there) gives them a fixed time
-            if (rank == 0) {
-                for (int s = 0; s < kPStages; ++s)
-                    if (issued_mask & (1u << s))
-                        ptx::mbar_wait_cluster(ptx::smem_addr(&sh->full[s]), (issued_parity >> s) & 1u,
-                                               ptx::globaltimer() + kWaitNs);
-            } else {
-                const uint64_t until = ptx::globaltimer() + 1000000ull;
-                while (ptx::globaltimer() < until) __nanosleep(1000);
-            }
-        }
-    } else if (warp == 1 && lane == 0 && rank == 0) {
-        // ------------------------------------------------ MMA issuer (even CTA, for the pair)
-        constexpr uint32_t idesc = ptx::idesc_e4m3_e2m1(2 * kBlockM, kBN);
-        const uint32_t tfull_addr = ptx::smem_addr(&sh->tmem_full);
-        int stage = 0;
-        uint32_t phase = 0, acc_phase = 0;
-        bool ok = true;
-        for (int w = cluster; w < n_work && ok; w += n_clusters) {
-            if (pair_aborted(sh) ||
-                !pair_wait_or_abort(ptx::smem_addr(&sh->tmem_empty), acc_phase ^ 1, sh, p.err, 16))
-                break;
-            ptx::tc_fence_after();
-            for (int kb = 0; kb < kb_count; ++kb) {
-                if (pair_aborted(sh) ||
-                    !pair_wait_or_abort(ptx::smem_addr(&sh->full[stage]), phase, sh, p.err, 32 + stage)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t st = ptx::smem_addr(smem + stage * kPStageStride);
-                const uint32_t tsf = tmem + kSfTmemCol + 16 * stage;
-                ptx::tc_cp_32x128b_warpx4_pair(tsf + 0, ptx::desc_sf_32x16(st + kPSfaOff));
-                ptx::tc_cp_32x128b_warpx4_pair(tsf + 4, ptx::desc_sf_32x16(st + kPSfbOff));
-                ptx::tc_cp_32x128b_warpx4_pair(tsf + 8, ptx::desc_sf_32x16(st + kPSfbOff + kSfChunkBytes));
-#pragma unroll
-                for (int kk = 0; kk < kBlockK / 32; ++kk) {
-                    const uint64_t a_desc = ptx::desc_kmajor_sw128(st + kk * 32);
-                    const uint64_t b_desc = ptx::desc_kmajor_sw128(st + kABytes + kk * 32);
-                    ptx::mma_mxf8f6f4_pair(tmem, a_desc, b_desc, ptx::idesc_with_sf_id(idesc, kk), tsf + 0, tsf + 4,
-                                           (kb | kk) != 0);
-                }
-                ptx::tc_commit_pair(ptx::map_to_rank(ptx::smem_addr(&sh->empty[stage]), 0));
-                ptx::tc_commit_pair(ptx::map_to_rank(ptx::smem_addr(&sh->empty[stage]), 1));
-                if (++stage == kPStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-            }
-            if (!ok) break;
-            ptx::tc_commit_pair(ptx::map_to_rank(tfull_addr, 0));
-            ptx::tc_commit_pair(ptx::map_to_rank(tfull_addr, 1));
-            acc_phase ^= 1;
-        }
-        // all tensor-core work of the pair done before tensor memory is freed
-        ptx::tc_commit_pair(ptx::map_to_rank(ptx::smem_addr(&sh->drain), 0));
-        ptx::mbar_wait_cluster(ptx::smem_addr(&sh->drain), 0, ptx::globaltimer() + kWaitNs);
-    } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue (both CTAs)
-        const int quad = warp & 3;
-        const int half = (warp - 2) / 4;
-        const int m = quad * 32 + lane;
-        const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-        const uint32_t release_addr = ptx::map_to_rank(ptx::smem_addr(&sh->tmem_empty), 0);
-        uint32_t acc_phase = 0;
-        for (int w = cluster; w < n_work; w += n_clusters) {
-            const int pe = __ldg(p.pair_block + w / p.n_tiles), j = w % p.n_tiles;
-            const bool own_rows = rank == 0 || (pe & 1) != 0;
-            const int b = (pe >> 1) + static_cast<int>(rank);
-            const int r = b * kBlockM + m;
-            const int tok = own_rows ? __ldg(p.row_token + r) : -1;
-            const float wgt = own_rows ? __ldg(p.row_weight + r) : 0.0f;
-            const bool go =
-                !pair_aborted(sh) && pair_wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p.err, 48);
-            if (!__all_sync(0xffffffffu, go)) break;
-            ptx::tc_fence_after();
-            uint32_t pk[64];
-            drain_accumulator<kLayer>(t_row, half, pk, [&] {
-                if (lane == 0) ptx::mbar_arrive_cluster(release_addr);
-            });
-            if (tok >= 0) store_tile_row<kLayer>(p, b, j, r, quad, half, lane, wgt, pk);
-            acc_phase ^= 1;
-        }
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::cluster_sync();  // the pair's MMAs are complete (the even CTA waited on `drain`)
-    if (warp == 1) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc_pair(tmem, kTmemCols);
-    }
-    ptx::cluster_sync();
 #else
     if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kDevErrTimeout);
 #endif
@@ -728,20 +494,6 @@ bool make_map_3d_fp4(CUtensorMap* map, const void* base, uint64_t k_elems, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scale chunks seen by TMA as rows of 256 bytes: a box of `box_rows` rows
-// brings box_rows / 2 consecutive 512-byte chunks.
-bool make_sf_map(CUtensorMap* map, const void* base, uint64_t bytes, uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {256, bytes / 256};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {256, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 namespace {
@@ -749,7 +501,7 @@ namespace {
 // Opt a kernel into its dynamic shared memory once per device.
 template <typename Kernel>
 cudaError_t smem_attr_once(Kernel kernel, int slot, int bytes) {
-    static int done[4][64] = {};
+    static int done[2][64] = {};
     int dev = 0;
     cudaError_t st = cudaGetDevice(&dev);
     if (st != cudaSuccess) return st;
@@ -765,7 +517,7 @@ namespace {
 
 // One CTA per SM, 128-row tiles: B arrives as one request per stage (a 3-D
 // map brings the gate and up rows for layer 1, a 256-row box for layer 2).
-cudaError_t launch_single(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
+cudaError_t launch_gemm(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
                           int num_sms, cudaStream_t s) {
     CUtensorMap map_a, map_b;
     bool maps_ok = make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, kBlockM);
@@ -777,44 +529,14 @@ cudaError_t launch_single(int layer, const Layout& L, const GemmLaunch& g, const
     if (!maps_ok) return cudaErrorInvalidValue;
     cudaError_t st;
     if (layer == 1) {
-        if ((st = smem_attr_once(expert_gemm_kernel<1>, 2, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<1><<<num_sms, kSingleThreads, kSmemBytes, s>>>(map_a, map_b, p);
+        if ((st = smem_attr_once(expert_gemm_kernel<1>, 0, kSmemBytes)) != cudaSuccess) return st;
+        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_b, p);
     } else {
-        if ((st = smem_attr_once(expert_gemm_kernel<2>, 3, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<2><<<num_sms, kSingleThreads, kSmemBytes, s>>>(map_a, map_b, p);
+        if ((st = smem_attr_once(expert_gemm_kernel<2>, 1, kSmemBytes)) != cudaSuccess) return st;
+        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_b, p);
     }
     return cudaGetLastError();
 }
-
-// CTA pairs (2-SM MMA), 256-row tiles over the pair table.
-cudaError_t launch_pair(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
-                        int num_sms, cudaStream_t s) {
-    const uint64_t kb_count = static_cast<uint64_t>(g.K) / kBlockK;
-    const uint64_t sfa_bytes = static_cast<uint64_t>(L.p_cap / kBlockM) * kb_count * kSfChunkBytes;
-    const uint64_t sfb_bytes = static_cast<uint64_t>(g.E) * ((g.N + 255) / 256) * kb_count * 2 * kSfChunkBytes;
-    // A: pool rows, 128-row boxes; B: all experts' weight rows [E*N, K],
-    // 128-row boxes (one half of the 256-row tile per CTA); scales as
-    // 256-byte rows (an SFA chunk = 2 rows, an SFB chunk pair = 4 rows).
-    CUtensorMap map_a, map_b, map_sfa, map_sfb;
-    const bool maps_ok =
-        make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, kBlockM) &&
-        make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K, static_cast<uint64_t>(g.E) * g.N, g.K / 2,
-                 kPBRows) &&
-        make_sf_map(&map_sfa, p.sfa, sfa_bytes, 2) && make_sf_map(&map_sfb, p.sfb, sfb_bytes, 4);
-    if (!maps_ok) return cudaErrorInvalidValue;
-    const int grid = std::max(2, num_sms / 2 * 2);
-    cudaError_t st;
-    if (layer == 1) {
-        if ((st = smem_attr_once(expert_gemm_pair_kernel<1>, 0, kPSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_pair_kernel<1><<<grid, kThreads, kPSmemBytes, s>>>(map_a, map_b, map_sfa, map_sfb, p);
-    } else {
-        if ((st = smem_attr_once(expert_gemm_pair_kernel<2>, 1, kPSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_pair_kernel<2><<<grid, kThreads, kPSmemBytes, s>>>(map_a, map_b, map_sfa, map_sfb, p);
-    }
-    return cudaGetLastError();
-}
-
-constexpr bool kUsePair = false;
 
 }  // namespace
 
@@ -824,8 +546,6 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     GemmParams p{};
     p.n_blocks = reinterpret_cast<const int*>(ws + L.n_blocks);
     p.block_expert = reinterpret_cast<const int*>(ws + L.block_expert);
-    p.pair_block = reinterpret_cast<const int*>(ws + L.pair_block);
-    p.n_pairs = reinterpret_cast<const int*>(ws + L.n_pairs);
     p.row_token = reinterpret_cast<const int*>(ws + L.row_token);
     p.row_weight = reinterpret_cast<const float*>(ws + L.row_weight);
     p.sfb = static_cast<const uint8_t*>(g.w_sf);
@@ -847,8 +567,7 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
         p.out_bf16 = reinterpret_cast<uint16_t*>(ws + L.l2_out);
         p.n_tiles = (L.H + kBN - 1) / kBN;
     }
-    return kUsePair ? launch_pair(layer, L, g, a_base, p, num_sms, s)
-                    : launch_single(layer, L, g, a_base, p, num_sms, s);
+    return launch_gemm(layer, L, g, a_base, p, num_sms, s);
 }
 
 }  // namespace moe

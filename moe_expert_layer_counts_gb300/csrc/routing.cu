@@ -98,9 +98,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
                                                                    int* __restrict__ poff,
                                                                    int* __restrict__ chunk_base,
                                                                    int* __restrict__ block_expert,
-                                                                   int* __restrict__ n_blocks,
-                                                                   int* __restrict__ pair_block,
-                                                                   int* __restrict__ n_pairs) {
+                                                                   int* __restrict__ n_blocks) {
     __shared__ int s_warp[32];
     const int e = threadIdx.x;
     int c_e = 0;
@@ -126,19 +124,6 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
         }
         const int b0 = (inc_p - padded) / kBlockM;
         for (int b = 0; b < padded / kBlockM; ++b) block_expert[b0 + b] = e;
-    }
-    // Pairs of row blocks of one expert for the 2-SM tensor-core tiles: an
-    // expert with nb blocks gives ceil(nb / 2) pairs; the last one of an odd
-    // nb has no second block.  Entry = 2 * first block + (second present).
-    if (pair_block != nullptr) {
-        const int nb = padded / kBlockM;
-        const int np = (nb + 1) / 2;
-        const int inc_q = block_inclusive_scan(np, s_warp);
-        if (e < E) {
-            const int b0 = (inc_p - padded) / kBlockM;
-            for (int q = 0; q < np; ++q) pair_block[inc_q - np + q] = 2 * (b0 + 2 * q) + (2 * q + 1 < nb ? 1 : 0);
-            if (e == E - 1) *n_pairs = inc_q;
-        }
     }
 }
 
@@ -217,9 +202,7 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
     }
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, L.chunks, L.E, count, off, poff, chunk_base,
                                                  reinterpret_cast<int*>(ws + L.block_expert),
-                                                 reinterpret_cast<int*>(ws + L.n_blocks),
-                                                 reinterpret_cast<int*>(ws + L.pair_block),
-                                                 reinterpret_cast<int*>(ws + L.n_pairs));
+                                                 reinterpret_cast<int*>(ws + L.n_blocks));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     if (L.chunks > 0) {
         const size_t smem = static_cast<size_t>(L.E) * (1 + kSlotWarps) * sizeof(int);
@@ -296,6 +279,6 @@ extern "C" int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, 
     }
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(scratch + kStaticHist, chunks, E, count, offsets, padded_offsets,
                                                  scratch + kStaticBase, scratch + kStaticBlocks,
-                                                 scratch + kStaticNBlocks, nullptr, nullptr);
+                                                 scratch + kStaticNBlocks);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
