@@ -139,8 +139,9 @@ def measured_traffic():
     return m.get("bytes_per_launch") if m.get("kernel_sha") == kernel_source_hash() else None
 
 
-def cpu_baseline(w, d, n_tokens: int):
-    """The oracle, as it stands, on the host cores: a bounded sample of tokens."""
+def cpu_baseline(w, d, target_s: float):
+    """The oracle, as it stands, on the host cores: an evenly spaced token
+    sample sized (from a 64-token calibration run) to about target_s seconds."""
     import numpy as np
     import oracle
     oracle.build()
@@ -148,11 +149,25 @@ def cpu_baseline(w, d, n_tokens: int):
     idx = d["topk_idx"].cpu().numpy()
     tw = d["topk_w"].cpu().numpy()
     ws = [d[n].cpu().numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
-    step = max(1, w.T // n_tokens)
-    toks = np.arange(0, w.T, step, dtype=np.int32)[:n_tokens]
+
+    def sample(n):
+        step = max(1, w.T // n)
+        return step, np.arange(0, w.T, step, dtype=np.int32)[:n]
+
+    _, toks = sample(min(w.T, 64))
     t0 = time.perf_counter()
     oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
-    dt = time.perf_counter() - t0
+    t_cal = time.perf_counter() - t0
+    n, dt = len(toks), t_cal
+    for _ in range(2):  # the time grows less than linearly (per-expert weight decoding), so refine once
+        if n >= w.T or dt >= 0.5 * target_s:
+            break
+        n = int(min(w.T, max(n + 1, n * target_s / max(dt, 1e-6))))
+        step, toks = sample(n)
+        t0 = time.perf_counter()
+        oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
+        dt = time.perf_counter() - t0
+    step, toks = sample(len(toks))
     n_valid = int((idx[toks] >= 0).sum())
     return dict(value=6.0 * n_valid * w.H * w.I / dt / 1e12, unit="TFLOP/s", cores=oracle.num_threads(),
                 kind="oracle", seconds=dt, tokens_per_s=len(toks) / dt,
@@ -202,7 +217,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="full", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample for cpu_baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU time the cpu_baseline sample aims at")
     ap.add_argument("--ref-tokens", type=int, default=1, help="oracle tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -302,7 +317,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, d, args.cpu_tokens)
+        cpu = cpu_baseline(w, d, args.cpu_seconds)
     if rank != 0:
         return
     line = dict(
