@@ -61,6 +61,10 @@ def lib():
             L.or_ue8m0_ceil.argtypes = [f64, f64]
             L.or_ue8m0_value.restype = f64
             L.or_ue8m0_value.argtypes = [i32]
+            L.or_ue8m0_floor.argtypes = [f64, i32]
+            L.or_ue8m0_floor.restype = i32
+            L.or_quant_mx_e4m3_rule.argtypes = [P, i32, P, P, i32]
+            L.or_quant_mx_e4m3_rule.restype = None
             L.or_bf16_decode.restype = ctypes.c_float
             L.or_bf16_decode.argtypes = [ctypes.c_uint16]
             L.or_bf16_encode.restype = ctypes.c_uint16
@@ -72,15 +76,16 @@ def lib():
             L.or_plan.restype = i32
             L.or_plan.argtypes = [P, P, i32, i32, i32, i64, P, P, P, P, P, P, P]
             L.or_quant_x.restype = None
-            L.or_quant_x.argtypes = [P, i32, i32, P, P, i32]
+            L.or_quant_x.argtypes = [P, i32, i32, i32, P, P, i32]
             L.or_forward.restype = i32
-            L.or_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P, i64, i32]
+            L.or_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P, i64,
+                                     ctypes.c_float, i32, i32]
             L.or_combine.restype = None
             L.or_combine.argtypes = [P, P, i32, i32, i32, P]
             L.or_l2_row.restype = None
             L.or_l2_row.argtypes = [P, P, P, P, i32, i32, i32, P]
             L.or_bruteforce_token.restype = i32
-            L.or_bruteforce_token.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, P]
+            L.or_bruteforce_token.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, ctypes.c_float, i32, P]
             L.or_num_threads.restype = i32
             L.or_num_threads.argtypes = []
             _lib = L
@@ -113,6 +118,15 @@ def e2m1_encode(v: float) -> int:
     return lib().or_e2m1_encode(float(v))
 
 
+SCALE_RULE_CEIL = 0
+SCALE_RULE_OCP_FLOOR = 1
+
+
+def ue8m0_floor(amax: float, emax_elem: int) -> int:
+    """UE8M0 byte of the OCP MX floor rule: 2^(floor(log2 amax) - emax_elem)."""
+    return lib().or_ue8m0_floor(float(amax), int(emax_elem))
+
+
 def ue8m0_ceil(amax: float, maxnorm: float) -> int:
     return lib().or_ue8m0_ceil(float(amax), float(maxnorm))
 
@@ -129,12 +143,12 @@ def bf16_encode(v: float) -> int:
     return lib().or_bf16_encode(float(v))
 
 
-def quant_mx_e4m3(v: np.ndarray):
-    """MXFP8 of a float32 vector (length multiple of 32) -> (codes u8, sf u8)."""
+def quant_mx_e4m3(v: np.ndarray, scale_rule: int = SCALE_RULE_CEIL):
+    """MX E4M3 of a float32 vector (length a multiple of 32) -> (codes, scale bytes)."""
     v = _c(v, np.float32).ravel()
     codes = np.zeros(v.size, np.uint8)
     sf = np.zeros(v.size // SF_VEC, np.uint8)
-    lib().or_quant_mx_e4m3(_p(v), v.size, _p(codes), _p(sf))
+    lib().or_quant_mx_e4m3_rule(_p(v), v.size, _p(codes), _p(sf), int(scale_rule))
     return codes, sf
 
 
@@ -176,23 +190,26 @@ def plan(topk_idx: np.ndarray, topk_w: np.ndarray, E: int, p_cap: int | None = N
     return out
 
 
-def quant_x(x_bf16_bits: np.ndarray, nthreads: int = 0):
+def quant_x(x_bf16_bits: np.ndarray, nthreads: int = 0, scale_rule: int = SCALE_RULE_CEIL):
     """Token-major MXFP8 of x given as uint16 bf16 bits [T,H] -> (q [T,H], sf [T,H/32])."""
     x = _c(x_bf16_bits, np.uint16)
     T, H = x.shape
     q = np.zeros((T, H), np.uint8)
     sf = np.zeros((T, H // SF_VEC), np.uint8)
-    lib().or_quant_x(_p(x), T, H, _p(q), _p(sf), nthreads)
+    lib().or_quant_x(_p(x), T, H, int(scale_rule), _p(q), _p(sf), nthreads)
     return q, sf
 
 
 def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
-            want_pool=False, nthreads: int = 0):
+            want_pool=False, nthreads: int = 0, activation_clamp: float = 0.0,
+            scale_rule: int = SCALE_RULE_CEIL):
     """Oracle forward.  x: uint16 bf16 bits [T,H]; w1q uint8 [E,2I,H/2]; w1sf uint8
     [E,2I,H/32]; w2q uint8 [E,H,I/2]; w2sf uint8 [E,H,I/32].
     tokens: optional int array of tokens to compute (y rows in that order).
     want_pool: also return per-pool-row hq [p_cap,I], hsf [p_cap,I/32], o [p_cap,H] and the
     pre-requantisation h [p_cap,I] (float32).
+    activation_clamp: > 0 limits the bf16 gate and up values to [-c, c] before SwiGLU.
+    scale_rule: SCALE_RULE_CEIL or SCALE_RULE_OCP_FLOOR for the activation (x and h) scales.
     Returns dict(y=uint16 bf16 bits, status, and pool arrays if asked)."""
     x = _c(x_bf16_bits, np.uint16)
     T, H = x.shape
@@ -220,7 +237,8 @@ def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
     st = lib().or_forward(_p(x), _p(idx), _p(w), T, k, E, H, I, _p(w1q), _p(w1sf), _p(w2q), _p(w2sf),
                           toks_p, ntok, _p(y),
                           _p(hq) if hq is not None else None, _p(hsf) if hsf is not None else None,
-                          _p(o) if o is not None else None, _p(hf) if hf is not None else None, p_cap, nthreads)
+                          _p(o) if o is not None else None, _p(hf) if hf is not None else None, p_cap,
+                          float(activation_clamp), int(scale_rule), nthreads)
     res.update(y=y, status=st)
     if hq is not None:
         res.update(hq=hq, hsf=hsf, o=o, h=hf)
@@ -248,7 +266,8 @@ def l2_row(hq_row, hsf_row, w2q, w2sf, e: int):
     return o
 
 
-def bruteforce_token(x_row_bits, idx_row, w_row, E, w1q, w1sf, w2q, w2sf):
+def bruteforce_token(x_row_bits, idx_row, w_row, E, w1q, w1sf, w2q, w2sf, activation_clamp: float = 0.0,
+                     scale_rule: int = SCALE_RULE_CEIL):
     x = _c(x_row_bits, np.uint16).ravel()
     idx = _c(idx_row, np.int64).ravel()
     w = _c(w_row, np.float32).ravel()
@@ -257,7 +276,7 @@ def bruteforce_token(x_row_bits, idx_row, w_row, E, w1q, w1sf, w2q, w2sf):
     I = w2q.shape[2] * 2
     y = np.zeros(H, np.uint16)
     st = lib().or_bruteforce_token(_p(x), _p(idx), _p(w), idx.size, E, H, I, _p(w1q), _p(w1sf),
-                                   _p(w2q), _p(w2sf), _p(y))
+                                   _p(w2q), _p(w2sf), float(activation_clamp), int(scale_rule), _p(y))
     return y, st
 
 

@@ -46,6 +46,8 @@
 
 #define OR_BLOCK_M 128 /* expert pool rows are aligned to one MMA row block */
 #define OR_SF_VEC 32   /* one UE8M0 scale per 32 elements (recipe 1,1,32)  */
+#define OR_RULE_CEIL 0      /* activation scale rule: smallest 2^e with amax <= max * 2^e */
+#define OR_RULE_OCP_FLOOR 1 /* activation scale rule: 2^(floor(log2 amax) - emax), saturating */
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -121,6 +123,22 @@ int or_ue8m0_ceil(double amax, double maxnorm) {
     return e + 127;
 }
 
+/* UE8M0 shared scale, OCP MX "floor" rule (OCP Microscaling Formats v1.0,
+ * section 6.3): X = 2^(floor(log2(amax)) - emax_elem), emax_elem = 8 for
+ * E4M3 (448 = 1.75 * 2^8) and 2 for E2M1 (6 = 1.5 * 2^2); scaled values
+ * beyond the largest normal saturate in the cast.  e clamped to [-126, 127];
+ * amax == 0 gives byte 127.  frexp gives amax = f * 2^q with f in [0.5, 1),
+ * so floor(log2(amax)) = q - 1 exactly. */
+int or_ue8m0_floor(double amax, int emax_elem) {
+    if (!(amax > 0.0)) return 127;
+    int q;
+    frexp(amax, &q);
+    int e = (q - 1) - emax_elem;
+    if (e < -126) e = -126;
+    if (e > 127) e = 127;
+    return e + 127;
+}
+
 double or_ue8m0_value(int byte) { return ldexp(1.0, byte - 127); }
 
 /* bfloat16: upper half of an IEEE binary32.  Round to nearest even on the
@@ -144,16 +162,20 @@ uint16_t or_bf16_encode(float f) {
 /* MX quantisation of n values (n a multiple of 32) to E4M3 codes with one
  * UE8M0 byte per 32 ([P1] amax reduction + __nv_fp8x4_e4m3 cast; recipe
  * (1,1,32) of [P2] section 2). */
-void or_quant_mx_e4m3(const float* v, int n, uint8_t* codes, uint8_t* sf) {
+void or_quant_mx_e4m3_rule(const float* v, int n, uint8_t* codes, uint8_t* sf, int rule) {
     for (int b = 0; b < n / OR_SF_VEC; ++b) {
         double amax = 0.0;
         for (int i = 0; i < OR_SF_VEC; ++i) amax = fmax(amax, fabs((double)v[b * OR_SF_VEC + i]));
-        int byte = or_ue8m0_ceil(amax, 448.0);
+        int byte = rule == OR_RULE_OCP_FLOOR ? or_ue8m0_floor(amax, 8) : or_ue8m0_ceil(amax, 448.0);
         sf[b] = (uint8_t)byte;
         double inv = ldexp(1.0, 127 - byte);
         for (int i = 0; i < OR_SF_VEC; ++i)
             codes[b * OR_SF_VEC + i] = (uint8_t)or_e4m3_encode((double)v[b * OR_SF_VEC + i] * inv);
     }
+}
+
+void or_quant_mx_e4m3(const float* v, int n, uint8_t* codes, uint8_t* sf) {
+    or_quant_mx_e4m3_rule(v, n, codes, sf, OR_RULE_CEIL);
 }
 
 /* Same for E2M1 (maxnorm 6); nibbles returned one per byte. */
@@ -233,6 +255,17 @@ static void dequant_expert(const uint8_t* q, const uint8_t* sf, int e, int N, in
     }
 }
 
+/* The optional activation clamp ("activation_clamp" of the API on the
+ * "Normal vs Low-Latency" page, whose meaning the pages do not spell out):
+ * c > 0 limits the bf16-rounded gate and up values to [-c, c] before
+ * SwiGLU; c <= 0 leaves them unchanged. */
+static float clamp_act(float v, float c) {
+    if (!(c > 0.0f)) return v;
+    if (v > c) return c;
+    if (v < -c) return -c;
+    return v;
+}
+
 /* One (token, expert) row of the FFN.
  *   xq/xsf : the token's E4M3 codes [H] and UE8M0 bytes [H/32]
  *   w1d    : dequantised W1 of the expert [2I, H]   (gate rows 0..I-1, up I..2I-1)
@@ -240,7 +273,7 @@ static void dequant_expert(const uint8_t* q, const uint8_t* sf, int e, int N, in
  *   weight : the top-k weight of this (token, j) entry
  * Outputs: hq[I] / hsf[I/32] (requantised SwiGLU*w), o[H] (bf16 bits). */
 static void ffn_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, const float* w2d,
-                    int H, int I, float weight, double* xd, double* hd, float* h,
+                    int H, int I, float weight, float clamp, int rule, double* xd, double* hd, float* h,
                     uint8_t* hq, uint8_t* hsf, uint16_t* o) {
     for (int c = 0; c < H; ++c) xd[c] = or_e4m3_decode(xq[c]) * or_ue8m0_value(xsf[c / OR_SF_VEC]);
     /* L1: gate and up accumulators, double sum -> fp32 -> bf16 */
@@ -249,15 +282,15 @@ static void ffn_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, con
         const float* wg = w1d + (size_t)n * H;
         const float* wu = w1d + (size_t)(I + n) * H;
         for (int c = 0; c < H; ++c) { ag += xd[c] * (double)wg[c]; au += xd[c] * (double)wu[c]; }
-        float g = or_bf16_decode(or_bf16_encode((float)ag));
-        float u = or_bf16_decode(or_bf16_encode((float)au));
+        float g = clamp_act(or_bf16_decode(or_bf16_encode((float)ag)), clamp);
+        float u = clamp_act(or_bf16_decode(or_bf16_encode((float)au)), clamp);
         /* SwiGLU in fp32: (gate * 1/(1+exp(-gate))) * up, then * topk weight */
         float silu = (float)((double)g / (1.0 + exp(-(double)g)));
         float hu = silu * u;
         h[n] = hu * weight;
     }
     /* requantise to MXFP8 along I */
-    or_quant_mx_e4m3(h, I, hq, hsf);
+    or_quant_mx_e4m3_rule(h, I, hq, hsf, rule);
     for (int i = 0; i < I; ++i) hd[i] = or_e4m3_decode(hq[i]) * or_ue8m0_value(hsf[i / OR_SF_VEC]);
     /* L2: double sum -> fp32 -> bf16, unweighted */
     for (int c = 0; c < H; ++c) {
@@ -269,7 +302,7 @@ static void ffn_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, con
 }
 
 /* Token-major MXFP8 quantisation of x (bf16 bits [T,H]). */
-void or_quant_x(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* sf, int nthreads) {
+void or_quant_x(const uint16_t* x, int T, int H, int rule, uint8_t* q, uint8_t* sf, int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
@@ -279,7 +312,7 @@ void or_quant_x(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* sf, int nt
 #pragma omp for schedule(static)
         for (int t = 0; t < T; ++t) {
             for (int c = 0; c < H; ++c) row[c] = or_bf16_decode(x[(size_t)t * H + c]);
-            or_quant_mx_e4m3(row, H, q + (size_t)t * H, sf + (size_t)t * (H / OR_SF_VEC));
+            or_quant_mx_e4m3_rule(row, H, q + (size_t)t * H, sf + (size_t)t * (H / OR_SF_VEC), rule);
         }
         free(row);
     }
@@ -297,7 +330,7 @@ int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
                const uint8_t* w1q, const uint8_t* w1sf, const uint8_t* w2q, const uint8_t* w2sf,
                const int32_t* tokens, int ntok, uint16_t* y,
                uint8_t* hq_pool, uint8_t* hsf_pool, uint16_t* o_pool, float* h_pool, int64_t p_cap,
-               int nthreads) {
+               float clamp, int rule, int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #endif
@@ -328,7 +361,7 @@ int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
         for (int t = 0; t < T; ++t) {
             if (want[t] < 0) continue;
             for (int c = 0; c < H; ++c) row[c] = or_bf16_decode(x[(size_t)t * H + c]);
-            or_quant_mx_e4m3(row, H, xq + (size_t)t * H, xsf + (size_t)t * (H / OR_SF_VEC));
+            or_quant_mx_e4m3_rule(row, H, xq + (size_t)t * H, xsf + (size_t)t * (H / OR_SF_VEC), rule);
         }
         free(row);
     }
@@ -359,7 +392,7 @@ int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
                 int32_t r = rows[ir];
                 int t = row_token[r], j = row_topk[r];
                 ffn_row(xq + (size_t)t * H, xsf + (size_t)t * (H / OR_SF_VEC), w1d, w2d, H, I,
-                        row_weight[r], xd, hd, h, hq, hsf, o);
+                        row_weight[r], clamp, rule, xd, hd, h, hq, hsf, o);
                 memcpy(o_ent + ((size_t)want[t] * k + j) * H, o, sizeof(uint16_t) * H);
                 if (!tokens) {
                     if (hq_pool) memcpy(hq_pool + (size_t)r * I, hq, (size_t)I);
@@ -434,7 +467,7 @@ void or_l2_row(const uint8_t* hq, const uint8_t* hsf, const uint8_t* w2q, const 
 /* ------------------------------------------------------------------------ */
 int or_bruteforce_token(const uint16_t* x_row, const int64_t* idx_row, const float* w_row, int k, int E,
                         int H, int I, const uint8_t* w1q, const uint8_t* w1sf,
-                        const uint8_t* w2q, const uint8_t* w2sf, uint16_t* y_row) {
+                        const uint8_t* w2q, const uint8_t* w2sf, float clamp, int rule, uint16_t* y_row) {
     float* xf = (float*)malloc(sizeof(float) * H);
     uint8_t* xq = (uint8_t*)malloc(H);
     uint8_t* xsf = (uint8_t*)malloc(H / OR_SF_VEC + 1);
@@ -444,7 +477,7 @@ int or_bruteforce_token(const uint16_t* x_row, const int64_t* idx_row, const flo
     float* acc_y = (float*)calloc(H, sizeof(float));
     int bad = 0;
     for (int c = 0; c < H; ++c) xf[c] = or_bf16_decode(x_row[c]);
-    or_quant_mx_e4m3(xf, H, xq, xsf);
+    or_quant_mx_e4m3_rule(xf, H, xq, xsf, rule);
     for (int j = 0; j < k; ++j) {
         int64_t e = idx_row[j];
         if (e < -1 || e >= E) { bad = 1; continue; }
@@ -460,13 +493,13 @@ int or_bruteforce_token(const uint16_t* x_row, const int64_t* idx_row, const flo
                 ag += a * or_e2m1_decode(ng) * or_ue8m0_value(w1sf[rg * (H / OR_SF_VEC) + c / OR_SF_VEC]);
                 au += a * or_e2m1_decode(nu) * or_ue8m0_value(w1sf[ru * (H / OR_SF_VEC) + c / OR_SF_VEC]);
             }
-            float g = or_bf16_decode(or_bf16_encode((float)ag));
-            float u = or_bf16_decode(or_bf16_encode((float)au));
+            float g = clamp_act(or_bf16_decode(or_bf16_encode((float)ag)), clamp);
+            float u = clamp_act(or_bf16_decode(or_bf16_encode((float)au)), clamp);
             float silu = (float)((double)g / (1.0 + exp(-(double)g)));
             float hu = silu * u;
             h[n] = hu * w_row[j];
         }
-        or_quant_mx_e4m3(h, I, hq, hsf);
+        or_quant_mx_e4m3_rule(h, I, hq, hsf, rule);
         for (int c = 0; c < H; ++c) {
             double acc = 0.0;
             size_t r2 = (size_t)e * H + c;
