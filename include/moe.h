@@ -132,17 +132,46 @@ int moe_prepare_weight_scales(const void* sf, int E, int N, int K, int pairing, 
 int moe_plan(moe_plan_t* plan, const int64_t* topk_idx, const float* topk_w, int T, int k, int E,
              int H, int I, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Layer options (the activation_clamp and fast_math arguments of the API on
+ * the Normal-vs-Low-Latency page; the pages define neither, so the readings
+ * are stated here).  Pass NULL for the defaults {0, MOE_SCALE_CEIL, 1}.
+ *   activation_clamp  > 0: the bf16-rounded gate and up values are limited to
+ *                     [-c, c] before SwiGLU; 0 or +inf: no clamp (NaN and
+ *                     negative values are MOE_ERR_INVALID_ARG)
+ *   scale_rule        UE8M0 rule of the activation scales (x in dispatch, h in
+ *                     the L1 epilogue): MOE_SCALE_CEIL = the smallest 2^e with
+ *                     amax <= 448 * 2^e; MOE_SCALE_OCP_FLOOR = OCP MX v1.0,
+ *                     2^(floor(log2 amax) - 8), values beyond 448 saturate
+ *   fast_math         1: SwiGLU with __expf and an approximate divide, every
+ *                     value recomputed exactly where that could change an E4M3
+ *                     code or a scale (so the result equals the exact
+ *                     formula's); 0: every value by the exact formula.  Both
+ *                     give the same bytes; 0 is slower. */
+enum {
+    MOE_SCALE_CEIL = 0,
+    MOE_SCALE_OCP_FLOOR = 1
+};
+typedef struct moe_options_t {
+    float activation_clamp;
+    int32_t scale_rule;
+    int32_t fast_math;
+    int32_t reserved[5]; /* must be zero */
+} moe_options_t;
+
 /* Dispatch gather (Dispatch/Combine page section 3.1, token pull into the
  * expert pool; recipe (1,1,32) of the Normal-vs-Low-Latency page section 2):
- * for each valid entry, pool row slot = MXFP8(x[t]).  x [T, H] bf16. */
-int moe_dispatch(const moe_plan_t* plan, const void* x, void* stream);
+ * for each valid entry, pool row slot = MXFP8(x[t]) with opts->scale_rule.
+ * x [T, H] bf16; opts may be NULL. */
+int moe_dispatch(const moe_plan_t* plan, const void* x, const moe_options_t* opts, void* stream);
 
 /* Expert L1 (DeepEP -> Mega MoE page, sm100_fp8_fp4_mega_moe.cuh snippets:
  * block-scaled FP8 x FP4 MMA, SwiGLU, amax, FP8 requant): for every pool row
  * block, tcgen05 block-scaled MMA over H, then the epilogue
- * h = silu(bf16(gate)) * bf16(up) * topk_weight, requantised to MXFP8.
+ * h = silu(bf16(gate)) * bf16(up) * topk_weight, requantised to MXFP8
+ * (gate and up clamped, the scale rule and fast_math as in moe_options_t;
+ * opts may be NULL).
  * W1: E, N = 2I, K = H must match the plan. */
-int moe_expert_l1(const moe_plan_t* plan, const moe_weights_t* W1, void* stream);
+int moe_expert_l1(const moe_plan_t* plan, const moe_weights_t* W1, const moe_options_t* opts, void* stream);
 
 /* Expert L2: pool rows of h x W2^T, fp32 accumulate, rounded to bf16 rows in
  * pool order (Dispatch/Combine page section 5.1, the unweighted bf16
@@ -156,9 +185,9 @@ int moe_expert_l2(const moe_plan_t* plan, const moe_weights_t* W2, void* stream)
 int moe_combine(const moe_plan_t* plan, void* y, void* stream);
 
 /* The whole layer after moe_plan(): moe_dispatch + moe_expert_l1 +
- * moe_expert_l2 + moe_combine, in stream order. */
+ * moe_expert_l2 + moe_combine, in stream order; opts may be NULL. */
 int moe_forward(const void* x, const moe_weights_t* W1, const moe_weights_t* W2,
-                const moe_plan_t* plan, void* y, void* stream);
+                const moe_plan_t* plan, void* y, const moe_options_t* opts, void* stream);
 
 /* Synchronises `stream`, then returns the first device-side error recorded
  * in the plan's workspace (MOE_ERR_BAD_EXPERT_ID, MOE_ERR_TIMEOUT) or

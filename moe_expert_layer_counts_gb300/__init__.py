@@ -66,6 +66,25 @@ class Weights(ctypes.Structure):
                 ("N", ctypes.c_int32), ("K", ctypes.c_int32)]
 
 
+SCALE_CEIL = 0
+SCALE_OCP_FLOOR = 1
+
+
+class Options(ctypes.Structure):
+    """moe_options_t: activation_clamp (> 0 limits bf16 gate/up to [-c, c]; 0 = off),
+    scale_rule (SCALE_CEIL / SCALE_OCP_FLOOR for the activation scales), fast_math
+    (1: fast SwiGLU with exact decisions, 0: exact everywhere; same bytes)."""
+    _fields_ = [("activation_clamp", ctypes.c_float), ("scale_rule", ctypes.c_int32),
+                ("fast_math", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+
+    def __init__(self, activation_clamp: float = 0.0, scale_rule: int = SCALE_CEIL, fast_math: int = 1):
+        super().__init__(float(activation_clamp), int(scale_rule), int(fast_math))
+
+
+def _opts(options: "Options | None"):
+    return None if options is None else ctypes.byref(options)
+
+
 def lib():
     """Load libmoe.so (it must have been built: see build.py)."""
     global _lib
@@ -83,14 +102,18 @@ def lib():
             L.moe_prepare_weight_scales.argtypes = [P, i32, i32, i32, i32, P, sz, P]
             L.moe_plan.restype = i32
             L.moe_plan.argtypes = [ctypes.POINTER(Plan), P, P, i32, i32, i32, i32, i32, P, sz, P]
-            for name in ("moe_dispatch", "moe_combine"):
-                getattr(L, name).restype = i32
-                getattr(L, name).argtypes = [ctypes.POINTER(Plan), P, P]
-            for name in ("moe_expert_l1", "moe_expert_l2"):
-                getattr(L, name).restype = i32
-                getattr(L, name).argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights), P]
+            OP = ctypes.POINTER(Options)
+            L.moe_dispatch.restype = i32
+            L.moe_dispatch.argtypes = [ctypes.POINTER(Plan), P, OP, P]
+            L.moe_combine.restype = i32
+            L.moe_combine.argtypes = [ctypes.POINTER(Plan), P, P]
+            L.moe_expert_l1.restype = i32
+            L.moe_expert_l1.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights), OP, P]
+            L.moe_expert_l2.restype = i32
+            L.moe_expert_l2.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights), P]
             L.moe_forward.restype = i32
-            L.moe_forward.argtypes = [P, ctypes.POINTER(Weights), ctypes.POINTER(Weights), ctypes.POINTER(Plan), P, P]
+            L.moe_forward.argtypes = [P, ctypes.POINTER(Weights), ctypes.POINTER(Weights), ctypes.POINTER(Plan), P,
+                                      OP, P]
             L.moe_plan_check.restype = i32
             L.moe_plan_check.argtypes = [ctypes.POINTER(Plan), P]
             L.moe_plan_export.restype = i32
@@ -200,13 +223,14 @@ def plan(topk_idx: torch.Tensor, topk_w: torch.Tensor, E: int, H: int, I: int,
     return MoePlan(p, workspace, T, k, E, H, I)
 
 
-def dispatch(p: MoePlan, x: torch.Tensor, stream=None):
+def dispatch(p: MoePlan, x: torch.Tensor, options: Options | None = None, stream=None):
     assert x.dtype == torch.bfloat16 and x.is_contiguous()
-    _check(lib().moe_dispatch(ctypes.byref(p.c), _ptr(x), _stream(stream)), "moe_dispatch")
+    _check(lib().moe_dispatch(ctypes.byref(p.c), _ptr(x), _opts(options), _stream(stream)), "moe_dispatch")
 
 
-def expert_l1(p: MoePlan, W1: MXFP4Weight, stream=None):
-    _check(lib().moe_expert_l1(ctypes.byref(p.c), ctypes.byref(W1.c), _stream(stream)), "moe_expert_l1")
+def expert_l1(p: MoePlan, W1: MXFP4Weight, options: Options | None = None, stream=None):
+    _check(lib().moe_expert_l1(ctypes.byref(p.c), ctypes.byref(W1.c), _opts(options), _stream(stream)),
+           "moe_expert_l1")
 
 
 def expert_l2(p: MoePlan, W2: MXFP4Weight, stream=None):
@@ -219,13 +243,13 @@ def combine(p: MoePlan, y: torch.Tensor, stream=None):
 
 
 def forward(x: torch.Tensor, W1: MXFP4Weight, W2: MXFP4Weight, p: MoePlan, y: torch.Tensor | None = None,
-            stream=None) -> torch.Tensor:
+            options: Options | None = None, stream=None) -> torch.Tensor:
     """moe_forward: dispatch + L1 + L2 + combine.  Returns y [T,H] bf16."""
     if y is None:
         y = torch.empty_like(x)
     assert x.dtype == torch.bfloat16 and x.is_contiguous() and y.is_contiguous()
     _check(lib().moe_forward(_ptr(x), ctypes.byref(W1.c), ctypes.byref(W2.c), ctypes.byref(p.c), _ptr(y),
-                             _stream(stream)), "moe_forward")
+                             _opts(options), _stream(stream)), "moe_forward")
     return y
 
 

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 
 #include "internal.h"
@@ -88,6 +89,20 @@ int check_weights(const moe_weights_t* w, int E, int N, int K) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Options with defaults filled in; false if a field is out of range.
+bool read_options(const moe_options_t* opts, moe_options_t* o) {
+    *o = moe_options_t{0.0f, MOE_SCALE_CEIL, 1, {0, 0, 0, 0, 0}};
+    if (!opts) return true;
+    if (std::isnan(opts->activation_clamp) || opts->activation_clamp < 0.0f) return false;
+    if (opts->scale_rule != MOE_SCALE_CEIL && opts->scale_rule != MOE_SCALE_OCP_FLOOR) return false;
+    if (opts->fast_math != 0 && opts->fast_math != 1) return false;
+    for (int r : opts->reserved)
+        if (r != 0) return false;
+    *o = *opts;
+    if (std::isinf(o->activation_clamp)) o->activation_clamp = 0.0f;
+    return true;
+}
 
 }  // namespace
 
@@ -200,19 +215,23 @@ int moe_plan(moe_plan_t* plan, const int64_t* topk_idx, const float* topk_w, int
     return cuda_status(launch_route(L, ps.ws, topk_idx, topk_w, static_cast<cudaStream_t>(stream)));
 }
 
-int moe_dispatch(const moe_plan_t* plan, const void* x, void* stream) {
+int moe_dispatch(const moe_plan_t* plan, const void* x, const moe_options_t* opts, void* stream) {
     const PlanState* ps = plan_state(plan);
+    moe_options_t o;
     if (!ps || (ps->T > 0 && !x) || (reinterpret_cast<uintptr_t>(x) & 15u)) return MOE_ERR_INVALID_ARG;
+    if (!read_options(opts, &o)) return MOE_ERR_INVALID_ARG;
     Layout L;
     make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
     int rc = device_info(nullptr);
     if (rc) return rc;
-    return cuda_status(launch_dispatch(L, ps->ws, x, static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_dispatch(L, ps->ws, x, o.scale_rule, static_cast<cudaStream_t>(stream)));
 }
 
-static int expert_layer(int layer, const moe_plan_t* plan, const moe_weights_t* W, void* stream) {
+static int expert_layer(int layer, const moe_plan_t* plan, const moe_weights_t* W, const moe_options_t* opts,
+                        void* stream) {
     const PlanState* ps = plan_state(plan);
-    if (!ps) return MOE_ERR_INVALID_ARG;
+    moe_options_t o;
+    if (!ps || !read_options(opts, &o)) return MOE_ERR_INVALID_ARG;
     const int N = layer == 1 ? 2 * ps->I : ps->H;
     const int K = layer == 1 ? ps->H : ps->I;
     int rc = check_weights(W, ps->E, N, K);
@@ -221,16 +240,16 @@ static int expert_layer(int layer, const moe_plan_t* plan, const moe_weights_t* 
     if ((rc = device_info(&sms))) return rc;
     Layout L;
     make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
-    GemmLaunch g{W->q, W->sf_mma, W->E, W->N, W->K};
+    GemmLaunch g{W->q, W->sf_mma, W->E, W->N, W->K, o.activation_clamp, o.scale_rule, o.fast_math};
     return cuda_status(launch_expert_gemm(layer, L, ps->ws, g, sms, static_cast<cudaStream_t>(stream)));
 }
 
-int moe_expert_l1(const moe_plan_t* plan, const moe_weights_t* W1, void* stream) {
-    return expert_layer(1, plan, W1, stream);
+int moe_expert_l1(const moe_plan_t* plan, const moe_weights_t* W1, const moe_options_t* opts, void* stream) {
+    return expert_layer(1, plan, W1, opts, stream);
 }
 
 int moe_expert_l2(const moe_plan_t* plan, const moe_weights_t* W2, void* stream) {
-    return expert_layer(2, plan, W2, stream);
+    return expert_layer(2, plan, W2, nullptr, stream);
 }
 
 int moe_combine(const moe_plan_t* plan, void* y, void* stream) {
@@ -244,10 +263,12 @@ int moe_combine(const moe_plan_t* plan, void* y, void* stream) {
 }
 
 int moe_forward(const void* x, const moe_weights_t* W1, const moe_weights_t* W2, const moe_plan_t* plan, void* y,
-                void* stream) {
+                const moe_options_t* opts, void* stream) {
     int rc;
-    if ((rc = moe_dispatch(plan, x, stream))) return rc;
-    if ((rc = moe_expert_l1(plan, W1, stream))) return rc;
+    moe_options_t o;
+    if (!read_options(opts, &o)) return MOE_ERR_INVALID_ARG;
+    if ((rc = moe_dispatch(plan, x, &o, stream))) return rc;
+    if ((rc = moe_expert_l1(plan, W1, &o, stream))) return rc;
     if ((rc = moe_expert_l2(plan, W2, stream))) return rc;
     return moe_combine(plan, y, stream);
 }

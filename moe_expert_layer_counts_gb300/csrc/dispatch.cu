@@ -26,7 +26,7 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
                                                                    const int* __restrict__ slot_of,
                                                                    uint8_t* __restrict__ pool_q,
-                                                                   uint8_t* __restrict__ pool_sf) {
+                                                                   uint8_t* __restrict__ pool_sf, int scale_rule) {
     const int lane = threadIdx.x & 31;
     const int nseg = (H + kSeg - 1) / kSeg;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const uint32_t sbyte = ue8m0_scale_e4m3(amax);
+        const uint32_t sbyte = ue8m0_scale_e4m3_rule(amax, scale_rule);
         const float inv = inv_scale_from_byte(sbyte);
         uint2 codes;
         codes.x = e4m3x2(f[0] * inv, f[1] * inv) | (e4m3x2(f[2] * inv, f[3] * inv) << 16);
@@ -76,14 +76,14 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
 
 }  // namespace
 
-cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, cudaStream_t s) {
+cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, cudaStream_t s) {
     if (L.T == 0) return cudaSuccess;
     const int nseg = (L.H + kSeg - 1) / kSeg;
     const int64_t items = static_cast<int64_t>(L.T) * nseg;
     const int64_t blocks = (items + kThreads / 32 - 1) / (kThreads / 32);
     dispatch_quant_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
         static_cast<const uint16_t*>(x), L.T, L.H, L.k, reinterpret_cast<const int*>(ws + L.slot_of),
-        ws + L.pool_q, ws + L.pool_sf);
+        ws + L.pool_q, ws + L.pool_sf, scale_rule);
     return cudaGetLastError();
 }
 

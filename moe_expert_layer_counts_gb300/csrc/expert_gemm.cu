@@ -27,6 +27,8 @@
 // Every wait is bounded (a global-timer deadline); on expiry the CTA records
 // an error in the workspace, waits for its own copies in flight, releases
 // tensor memory and exits.
+#include <limits>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -74,6 +76,9 @@ struct GemmParams {
     int I;                  // layer 1: intermediate size
     int H;                  // layer 2: output columns
     int* err;
+    float clamp;            // layer 1: gate/up limit, +inf for none
+    int scale_rule;         // layer 1: 0 = ceil, 1 = OCP floor (scales of h)
+    int fast_math;          // layer 1: 0 = every SwiGLU value by the exact formula
 };
 
 struct Shared {
@@ -123,17 +128,21 @@ __device__ __noinline__ float silu_exact(float g) {
 // scale byte.
 constexpr uint32_t kDecisionUlps = 64;
 
+// The optional activation clamp: the bf16 gate / up value limited to
+// [-c, c] (c = +inf when off, which leaves every finite value unchanged).
+__device__ __forceinline__ float clamp_act(float v, float c) { return fminf(fmaxf(v, -c), c); }
+
 // Replace h[i] by its exact value for every bit i set in `mask` (rare; a
 // local copy keeps dynamic indexing off the fast path).
-__device__ __noinline__ void exact_fixup(const uint32_t* gu, float wgt, float* h, uint32_t mask) {
+__device__ __noinline__ void exact_fixup(const uint32_t* gu, float wgt, float clamp, float* h, uint32_t mask) {
     while (mask) {
         const int i = __ffs(mask) - 1;
         mask &= mask - 1;
-        h[i] = (silu_exact(bf16_lo(gu[i])) * bf16_hi(gu[i])) * wgt;
+        h[i] = (silu_exact(clamp_act(bf16_lo(gu[i]), clamp)) * clamp_act(bf16_hi(gu[i]), clamp)) * wgt;
     }
 }
 
-__device__ __forceinline__ void fixup(const uint32_t* gu, float wgt, float (&h)[32], uint32_t mask) {
+__device__ __forceinline__ void fixup(const uint32_t* gu, float wgt, float clamp, float (&h)[32], uint32_t mask) {
     uint32_t gl[32];
     float hl[32];
 #pragma unroll
@@ -141,39 +150,40 @@ __device__ __forceinline__ void fixup(const uint32_t* gu, float wgt, float (&h)[
         gl[i] = gu[i];
         hl[i] = h[i];
     }
-    exact_fixup(gl, wgt, hl, mask);
+    exact_fixup(gl, wgt, clamp, hl, mask);
 #pragma unroll
     for (int i = 0; i < 32; ++i) h[i] = hl[i];
 }
 
-__device__ __forceinline__ uint32_t requant_block(const uint32_t* gu, float wgt, uint8_t* dst) {
+__device__ __forceinline__ uint32_t requant_block(const uint32_t* gu, float wgt, uint8_t* dst, float clamp,
+                                                  int scale_rule, int fast_math) {
     // 1. fast path, straight-line: values, block maximum, values it cannot decide
     float h[32];
-    uint32_t big = 0;
+    uint32_t big = fast_math ? 0u : 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const float g = bf16_lo(gu[i]), u = bf16_hi(gu[i]);
+        const float g = clamp_act(bf16_lo(gu[i]), clamp), u = clamp_act(bf16_hi(gu[i]), clamp);
         h[i] = (__fdividef(g, 1.0f + __expf(-g)) * u) * wgt;
         big |= static_cast<uint32_t>(fabsf(g) > 16.0f) << i;
     }
-    if (big) fixup(gu, wgt, h, big);
+    if (big) fixup(gu, wgt, clamp, h, big);
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-    // 2. the scale: if the maximum sits near the boundary, the whole block goes exact
-    if (near_e4m3_scale_boundary(amax, kDecisionUlps)) {
-        fixup(gu, wgt, h, 0xFFFFFFFFu);
+    // 2. the scale: if the maximum sits near the rule's boundary, the whole block goes exact
+    if (scale_rule ? near_pow2(amax, kDecisionUlps) : near_e4m3_scale_boundary(amax, kDecisionUlps)) {
+        fixup(gu, wgt, clamp, h, 0xFFFFFFFFu);
         amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
     }
-    const uint32_t sbyte = ue8m0_scale_e4m3(amax);
+    const uint32_t sbyte = ue8m0_scale_e4m3_rule(amax, scale_rule);
     const float inv = inv_scale_from_byte(sbyte);
     // 3. the codes: values near a rounding midpoint go exact
     uint32_t near = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) near |= static_cast<uint32_t>(near_e4m3_midpoint(h[i] * inv, kDecisionUlps)) << i;
-    if (near) fixup(gu, wgt, h, near);
+    if (near) fixup(gu, wgt, clamp, h, near);
     uint32_t q[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -223,8 +233,8 @@ __device__ __forceinline__ void store_tile_row(const GemmParams& p, int b, int j
     if (kLayer == 1) {
         // intermediate columns j*128 + 64*half + [0, 64): two 32-blocks
         uint8_t* dst = p.out_q + static_cast<size_t>(r) * p.I + j * 128 + 64 * half;
-        const uint32_t s0 = requant_block(pk, wgt, dst);
-        const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32);
+        const uint32_t s0 = requant_block(pk, wgt, dst, p.clamp, p.scale_rule, p.fast_math);
+        const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32, p.clamp, p.scale_rule, p.fast_math);
         const size_t chunk = static_cast<size_t>(b) * (p.I / 128) + j;
         *reinterpret_cast<uint16_t*>(p.out_sf + chunk * kSfChunkBytes + 16 * lane + 4 * quad + 2 * half) =
             static_cast<uint16_t>(s0 | (s1 << 8));
@@ -554,6 +564,9 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     p.I = L.I;
     p.H = L.H;
     p.err = reinterpret_cast<int*>(ws + L.err);
+    p.clamp = g.clamp > 0.0f ? g.clamp : std::numeric_limits<float>::infinity();  // no clamp
+    p.scale_rule = g.scale_rule;
+    p.fast_math = g.fast_math;
     const void* a_base;
     if (layer == 1) {
         a_base = ws + L.pool_q;

@@ -22,6 +22,24 @@ __device__ __forceinline__ uint32_t ue8m0_scale_e4m3(float amax) {
     return static_cast<uint32_t>(e + 127);
 }
 
+// The OCP MX v1.0 rule instead: X = 2^(floor(log2 amax) - 8) (8 = the
+// exponent of E4M3's largest normal, 448 = 1.75 * 2^8); scaled values beyond
+// 448 saturate in the cast.  floor(log2 amax) is the unbiased exponent field
+// of a normal amax; a subnormal amax gives the floor byte 1, 0 gives 127.
+__device__ __forceinline__ uint32_t ue8m0_scale_e4m3_floor(float amax) {
+    const uint32_t bits = __float_as_uint(amax) & 0x7FFFFFFFu;
+    if (bits == 0) return 127u;
+    const int ex = static_cast<int>(bits >> 23);
+    if (ex == 0) return 1u;
+    const int e = max(-126, min(127, (ex - 127) - 8));
+    return static_cast<uint32_t>(e + 127);
+}
+
+// Scale byte by rule (0 = ceil, 1 = OCP floor).
+__device__ __forceinline__ uint32_t ue8m0_scale_e4m3_rule(float amax, int rule) {
+    return rule ? ue8m0_scale_e4m3_floor(amax) : ue8m0_scale_e4m3(amax);
+}
+
 // 2^(127 - byte) for a scale byte in [1, 253] (always a normal float).
 __device__ __forceinline__ float inv_scale_from_byte(uint32_t byte) {
     return __uint_as_float((254u - byte) << 23);
@@ -72,6 +90,13 @@ __device__ __forceinline__ bool near_e4m3_scale_boundary(float amax, uint32_t ul
     const uint32_t m = __float_as_uint(amax) & 0x7FFFFFu;
     const uint32_t d = m > 0x600000u ? m - 0x600000u : 0x600000u - m;
     return d <= ulps;
+}
+
+// True when amax lies within `ulps` of a power of two (where the floor
+// rule's scale changes exponent).
+__device__ __forceinline__ bool near_pow2(float amax, uint32_t ulps) {
+    const uint32_t m = __float_as_uint(amax) & 0x7FFFFFu;
+    return m <= ulps || 0x800000u - m <= ulps;
 }
 
 // fp32 -> bf16 -> fp32 (round to nearest even).

@@ -48,7 +48,7 @@ constexpr uint64_t kPlanMagic = 0x4D6F45506C616E31ull;  // "MoEPlan1"
 // Launchers (enqueue only; return cudaError_t of the launch).
 cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, const float* topk_w,
                          cudaStream_t s);
-cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, cudaStream_t s);
+cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s);
 cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves, uint8_t* out, size_t out_bytes,
                               cudaStream_t s);
@@ -57,6 +57,9 @@ struct GemmLaunch {
     const void* w_q;      // packed e2m1 weights [E, N, K/2]
     const void* w_sf;     // tensor-core scale layout
     int E, N, K;
+    float clamp;          // layer 1: limit of the bf16 gate/up values (0 = none)
+    int scale_rule;       // layer 1: MOE_SCALE_CEIL or MOE_SCALE_OCP_FLOOR for h
+    int fast_math;        // layer 1: 1 = fast SwiGLU with exact decisions, 0 = exact everywhere
 };
 // layer 1: pool x W1 -> requantised h; layer 2: h x W2 -> bf16 rows.
 cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,

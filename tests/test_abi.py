@@ -64,8 +64,14 @@ def test_argument_errors_before_any_device_call(libmoe):
     # workspace too small
     assert libmoe.moe_plan(plan, 16, 16, 4, 2, 8, 256, 128, 256, 16, None) == 3
     libmoe.moe_forward.restype = ctypes.c_int
-    libmoe.moe_forward.argtypes = [ctypes.c_void_p] * 6
-    assert libmoe.moe_forward(None, None, None, plan, None, None) == 1  # plan never filled
+    libmoe.moe_forward.argtypes = [ctypes.c_void_p] * 7
+    assert libmoe.moe_forward(None, None, None, plan, None, None, None) == 1  # plan never filled
+    # options out of range are rejected before any device call
+    import moe_expert_layer_counts_gb300 as moe
+    assert ctypes.sizeof(moe.Options) == 32
+    for bad in (moe.Options(scale_rule=2), moe.Options(fast_math=3), moe.Options(activation_clamp=-1.0),
+                moe.Options(activation_clamp=float("nan"))):
+        assert libmoe.moe_forward(None, None, None, plan, None, ctypes.addressof(bad), None) == 1
     libmoe.moe_error_string.restype = ctypes.c_char_p
     for s in range(8):
         assert libmoe.moe_error_string(s)
