@@ -312,6 +312,35 @@ def main():
             e2e_ms += a.elapsed_time(b)
     e2e_t = max_over_ranks(e2e_ms / 1e3, world)
     e2e_val = world * flops * args.e2e_steps / e2e_t / 1e12
+
+    # the same step captured once in a CUDA graph (copies in, plan, forward, copy out) and replayed
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            gx.copy_(hx, non_blocking=True)
+            gidx.copy_(hidx, non_blocking=True)
+            gtw.copy_(htw, non_blocking=True)
+            gp = moe.plan(gidx, gtw, w.E, w.H, w.I, workspace=ws)
+            moe.forward(gx, W1, W2, gp, y)
+            hy.copy_(y, non_blocking=True)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph_ms = 0.0
+    for i in range(args.warmup + args.e2e_steps):
+        flush.fill_(3)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            graph_ms += a.elapsed_time(b)
+    status = moe.plan_check(gp)
+    assert status == 0, moe.error_string(status)
+    graph_t = max_over_ranks(graph_ms / 1e3, world)
+    graph_val = world * flops * args.e2e_steps / graph_t / 1e12
     h2d = hx.numel() * 2 + hidx.numel() * 8 + htw.numel() * 4
     d2h = hy.numel() * 2
 
@@ -341,7 +370,10 @@ def main():
                       algorithmic=f"4*N*H*I = {l1_flops:.4g} FLOP per launch (valid rows only)",
                       peak_note=f"FP8 = 2 x {pk['source']} sustained bf16 ({pk['bf16_sus']} TF/s)"),
         e2e=dict(value=e2e_val, unit="TFLOP/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                 ms_per_step=1e3 * e2e_t / args.e2e_steps),
+                 ms_per_step=1e3 * e2e_t / args.e2e_steps,
+                 graph=dict(value=graph_val, unit="TFLOP/s", ms_per_step=1e3 * graph_t / args.e2e_steps,
+                            note="the same step (copies in, plan, forward, copy out) captured once in a CUDA "
+                                 "graph and replayed")),
         gpu_launches=KERNELS_PER_STEP * args.steps,
         clocks=clk.summary(),
         cpu_baseline=cpu,
