@@ -244,6 +244,18 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
 int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, int E, int32_t* count, int32_t* offsets,
                               int32_t* padded_offsets, void* stream);
 
+/* Self-test of the device-side bounded wait that every pipeline barrier of
+ * the library uses (no counterpart on the pages; it exists so that failure
+ * detection can be exercised on a GPU without a fault).  One CTA waits on an
+ * mbarrier that `arrive` = 1 completes after about 20 us and `arrive` = 0
+ * leaves incomplete, giving up after timeout_ns of global time.
+ *   out  device int32[2], written by the kernel: {MOE_OK or MOE_ERR_TIMEOUT,
+ *        elapsed microseconds}
+ * Errors: MOE_ERR_INVALID_ARG (null out, timeout_ns of 0 or above 2 s),
+ * MOE_ERR_UNSUPPORTED (not an sm_103 device), MOE_ERR_CUDA.  The kernel never
+ * traps; after a time-out the context stays usable. */
+int moe_selftest_bounded_wait(int arrive, uint64_t timeout_ns, int32_t* out, void* stream);
+
 /* Static text for a status code. */
 const char* moe_error_string(int status);
 

@@ -46,7 +46,7 @@ _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_
 # every function declared in include/moe.h
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",
            "moe_dispatch", "moe_expert_l1", "moe_expert_l2", "moe_combine", "moe_forward", "moe_plan_check",
-           "moe_plan_export", "moe_error_string", "moe_expert_offsets_static")
+           "moe_plan_export", "moe_error_string", "moe_expert_offsets_static", "moe_selftest_bounded_wait")
 
 
 class MoeError(RuntimeError):
@@ -120,6 +120,8 @@ def lib():
             L.moe_plan_export.argtypes = [ctypes.POINTER(Plan), i32, ctypes.POINTER(sz), ctypes.POINTER(sz)]
             L.moe_expert_offsets_static.restype = i32
             L.moe_expert_offsets_static.argtypes = [P, i32, i32, i32, P, P, P, P]
+            L.moe_selftest_bounded_wait.restype = i32
+            L.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint64, P, P]
             L.moe_error_string.restype = ctypes.c_char_p
             L.moe_error_string.argtypes = [i32]
             _lib = L
@@ -271,3 +273,14 @@ def expert_offsets_static(topk_idx: torch.Tensor, E: int, stream=None):
     _check(lib().moe_expert_offsets_static(_ptr(topk_idx), T, k, E, _ptr(count), _ptr(off), _ptr(poff),
                                            _stream(stream)), "moe_expert_offsets_static")
     return count, off, poff
+
+
+def selftest_bounded_wait(arrive: bool, timeout_ns: int, stream=None):
+    """moe_selftest_bounded_wait: (status, elapsed_us) of one device-side bounded
+    mbarrier wait that is (arrive=True) or is not completed."""
+    out = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    _check(lib().moe_selftest_bounded_wait(int(bool(arrive)), int(timeout_ns), _ptr(out), _stream(stream)),
+           "moe_selftest_bounded_wait")
+    torch.cuda.synchronize()
+    st, us = (int(v) for v in out.cpu())
+    return st, us

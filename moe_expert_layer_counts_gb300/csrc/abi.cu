@@ -315,6 +315,14 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
     return MOE_OK;
 }
 
+int moe_selftest_bounded_wait(int arrive, uint64_t timeout_ns, int32_t* out, void* stream) {
+    if (!out || timeout_ns == 0 || timeout_ns > 2000000000ull || (arrive != 0 && arrive != 1))
+        return MOE_ERR_INVALID_ARG;
+    int rc = device_info(nullptr);
+    if (rc) return rc;
+    return cuda_status(launch_bounded_wait_selftest(arrive, timeout_ns, out, static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_error_string(int status) {
     switch (status) {
         case MOE_OK: return "ok";

@@ -53,6 +53,8 @@ cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStre
 cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves, uint8_t* out, size_t out_bytes,
                               cudaStream_t s);
 
+cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t timeout_ns, int32_t* out, cudaStream_t s);
+
 struct GemmLaunch {
     const void* w_q;      // packed e2m1 weights [E, N, K/2]
     const void* w_sf;     // tensor-core scale layout

@@ -1,0 +1,36 @@
+"""Failure detection without a GPU fault: the library's bounded mbarrier wait
+gives up at its deadline and reports MOE_ERR_TIMEOUT, and the context stays
+usable afterwards."""
+import numpy as np
+import pytest
+
+import gpu_helpers as gh
+from moe_expert_layer_counts_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_completes_when_arrived(moe):
+    st, us = moe.selftest_bounded_wait(True, 1_000_000_000)
+    assert st == moe.OK
+    assert 15 <= us < 100_000
+
+
+def test_bounded_wait_times_out_and_context_stays_usable(moe, oracle):
+    st, us = moe.selftest_bounded_wait(False, 20_000_000)   # 20 ms, nothing arrives
+    assert st == moe.ERR_TIMEOUT
+    assert 20_000 <= us < 500_000
+    # the GPU context is still good: a full forward runs and matches the oracle
+    w = inputs.WORKLOADS["tiny"]
+    d, W1, W2 = gh.setup(moe, w)
+    p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I)
+    y = moe.forward(d["x"], W1, W2, p)
+    assert moe.plan_check(p) == 0
+    ref = gh.oracle_forward(oracle, gh.host(d), w.E)["y"]
+    gh.assert_close_output(gh.bits(y), ref)
+
+
+def test_bounded_wait_argument_checks(moe):
+    for args in ((True, 0), (True, 3_000_000_000)):
+        with pytest.raises(moe.MoeError):
+            moe.selftest_bounded_wait(*args)
