@@ -341,6 +341,54 @@ def main():
     assert status == 0, moe.error_string(status)
     graph_t = max_over_ranks(graph_ms / 1e3, world)
     graph_val = world * flops * args.e2e_steps / graph_t / 1e12
+    # a stream of steps as a serving loop runs them: copies in, compute and copies out on three streams, two
+    # buffer sets, so step i+1's inputs arrive and step i-1's output leaves while step i computes (every step's
+    # copies stay inside the timed region; no L2 flush: the weights and the pool exceed L2 on these workloads)
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    gx2 = [torch.empty_like(d["x"]) for _ in range(2)]
+    gidx2 = [torch.empty_like(d["topk_idx"]) for _ in range(2)]
+    gtw2 = [torch.empty_like(d["topk_w"]) for _ in range(2)]
+    y2 = [torch.empty_like(d["x"]) for _ in range(2)]
+    hy2 = [torch.empty(w.T, w.H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(n):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_in.wait_stream(torch.cuda.current_stream())
+        start.record(s_in)
+        pl = None
+        for i in range(n):
+            b = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_in):
+                gx2[b].copy_(hx, non_blocking=True)
+                gidx2[b].copy_(hidx, non_blocking=True)
+                gtw2[b].copy_(htw, non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+            s_comp.wait_event(ev_in)
+            if i >= 2:
+                s_comp.wait_event(ev_out[b])
+            pl = moe.plan(gidx2[b], gtw2[b], w.E, w.H, w.I, workspace=ws, stream=s_comp)
+            moe.forward(gx2[b], W1, W2, pl, y2[b], stream=s_comp)
+            ev_comp[b].record(s_comp)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                hy2[b].copy_(y2[b], non_blocking=True)
+            ev_out[b].record(s_out)
+        end.record(s_out)
+        end.synchronize()
+        return start.elapsed_time(end), pl
+
+    pipelined(args.warmup)
+    torch.cuda.synchronize()
+    pipe_ms, pl = pipelined(args.e2e_steps)
+    status = moe.plan_check(pl, stream=s_comp)
+    assert status == 0, moe.error_string(status)
+    pipe_t = max_over_ranks(pipe_ms / 1e3, world)
+    pipe_val = world * flops * args.e2e_steps / pipe_t / 1e12
     h2d = hx.numel() * 2 + hidx.numel() * 8 + htw.numel() * 4
     d2h = hy.numel() * 2
 
@@ -369,11 +417,15 @@ def main():
                       unit="TFLOP/s", frac=l1_tf / fp8_sus, traffic=traffic,
                       algorithmic=f"4*N*H*I = {l1_flops:.4g} FLOP per launch (valid rows only)",
                       peak_note=f"FP8 = 2 x {pk['source']} sustained bf16 ({pk['bf16_sus']} TF/s)"),
-        e2e=dict(value=e2e_val, unit="TFLOP/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                 ms_per_step=1e3 * e2e_t / args.e2e_steps,
+        e2e=dict(value=pipe_val, unit="TFLOP/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                 ms_per_step=1e3 * pipe_t / args.e2e_steps,
+                 note="a stream of steps through the public API: each step copies its inputs in from pinned host "
+                      "memory and its y out; copies in, compute and copies out run on three streams with two "
+                      "buffer sets, so the copies of neighbouring steps overlap the compute",
+                 serial=dict(value=e2e_val, unit="TFLOP/s", ms_per_step=1e3 * e2e_t / args.e2e_steps,
+                             note="one step at a time: copy in, plan, forward, copy out, wait"),
                  graph=dict(value=graph_val, unit="TFLOP/s", ms_per_step=1e3 * graph_t / args.e2e_steps,
-                            note="the same step (copies in, plan, forward, copy out) captured once in a CUDA "
-                                 "graph and replayed")),
+                            note="one step at a time, captured once in a CUDA graph and replayed")),
         gpu_launches=KERNELS_PER_STEP * args.steps,
         clocks=clk.summary(),
         cpu_baseline=cpu,
