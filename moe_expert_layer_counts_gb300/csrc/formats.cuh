@@ -99,7 +99,4 @@ __device__ __forceinline__ bool near_pow2(float amax, uint32_t ulps) {
     return m <= ulps || 0x800000u - m <= ulps;
 }
 
-// fp32 -> bf16 -> fp32 (round to nearest even).
-__device__ __forceinline__ float round_bf16(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
-
 }  // namespace moe
