@@ -56,9 +56,9 @@ typedef enum moe_status {
     MOE_ERR_TOO_LARGE = 8      /* sizes exceed the fixed scratch of moe_expert_offsets_static() */
 } moe_status;
 
-/* Rows of one MMA tile; every expert's pool segment is padded to it
- * ("each expert's slots are aligned to BLOCK_M", Dispatch/Combine page,
- * Appendix A.2). */
+/* Rows of one MMA tile; every expert's pool segment is padded to a whole
+ * number of such row blocks (Dispatch/Combine page, Appendix A.2, where the
+ * block is BLOCK_M). */
 #define MOE_BLOCK_M 128
 
 /* Plan: caller-owned opaque storage, filled by moe_plan().  It records the

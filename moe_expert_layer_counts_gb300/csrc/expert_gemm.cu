@@ -9,7 +9,8 @@
 //
 // Layer 1: a work item is (pool row block b, intermediate tile j of 128).  The
 //   MMA has N = 256: weight rows gate [j*128, +128) and up [I + j*128, +128)
-//   are loaded as two TMA boxes into one B tile, so SwiGLU is tile-local.
+//   arrive in one 3-D TMA box (expert-half as the outer dimension) into one B
+//   tile, so SwiGLU is tile-local.
 //   Epilogue per pool row: g = bf16(acc_gate), u = bf16(acc_up),
 //   h = (g / (1 + exp(-g))) * u * topk_weight in fp32, requantised per 32 to
 //   E4M3 + UE8M0 (scales written in the tensor-core layout L2 reads).
