@@ -135,6 +135,7 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
     L->hist = take(sizeof(int) * static_cast<size_t>(chunks) * E);
     L->chunk_base = take(sizeof(int) * static_cast<size_t>(chunks) * E);
     L->block_expert = take(sizeof(int) * static_cast<size_t>(cap / kBlockM));
+    L->block_rows = take(sizeof(int) * static_cast<size_t>(cap / kBlockM));
     L->slot_of = take(sizeof(int) * static_cast<size_t>(std::max<int64_t>(n, 1)));
     L->row_token = take(sizeof(int) * static_cast<size_t>(cap));
     L->row_topk = take(sizeof(int) * static_cast<size_t>(cap));

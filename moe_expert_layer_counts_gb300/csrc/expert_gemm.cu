@@ -85,8 +85,7 @@ struct GemmParams {
     float clamp;            // layer 1: gate/up limit, +inf for none
     int scale_rule;         // layer 1: 0 = ceil, 1 = OCP floor (scales of h)
     int fast_math;          // layer 1: 0 = every SwiGLU value by the exact formula
-    const int* count;       // rows of each expert (plan)
-    const int* poff;        // padded row offset of each expert (plan)
+    const int* block_rows;  // valid rows of each pool row block (plan)
 };
 
 struct Shared {
@@ -302,18 +301,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
         const int pairs = (p.N + 255) / 256;
+        // the block metadata of the next work item is loaded one item ahead, so
+        // its latency never stalls the stream of copies at a tile boundary
+        int next_b = blockIdx.x / p.n_tiles;
+        int next_e = __ldg(p.block_expert + next_b);
+        int next_rows = __ldg(p.block_rows + next_b);
         for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-            const int b = w / p.n_tiles, j = w % p.n_tiles;
-            const int e = __ldg(p.block_expert + b);
+            const int b = next_b, j = w % p.n_tiles, e = next_e, rows = next_rows;
+            if (w + static_cast<int>(gridDim.x) < n_work) {
+                next_b = (w + static_cast<int>(gridDim.x)) / p.n_tiles;
+                next_e = __ldg(p.block_expert + next_b);
+                next_rows = __ldg(p.block_rows + next_b);
+            }
             // layer 1: gate|up halves of expert e, rows j*128 of each (3-D map: K, row, expert-half)
             // layer 2: rows e*H + 256*j .. +256 (2-D map)
             const int b_y = kLayer == 1 ? j * 128 : e * p.N + j * kBN;
             const int b_z = kLayer == 1 ? 2 * e : 0;
             const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
             const uint8_t* sfb = p.sfb + (static_cast<size_t>(e) * pairs + j) * kb_count * 2 * kSfChunkBytes;
-            // valid rows of this block: the expert's rows minus those of its earlier blocks
-            const int rows = __ldg(p.count + e) - (b * kBlockM - __ldg(p.poff + e));
-            const bool small = rows <= kSmallRows;
+            const bool small = rows <= kSmallRows;  // valid rows of the block
             for (int kb = 0; kb < kb_count; ++kb) {
                 if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
                     ok = false;
@@ -579,8 +585,7 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     p.I = L.I;
     p.H = L.H;
     p.err = reinterpret_cast<int*>(ws + L.err);
-    p.count = reinterpret_cast<const int*>(ws + L.count);
-    p.poff = reinterpret_cast<const int*>(ws + L.poff);
+    p.block_rows = reinterpret_cast<const int*>(ws + L.block_rows);
     p.clamp = g.clamp > 0.0f ? g.clamp : std::numeric_limits<float>::infinity();  // no clamp
     p.scale_rule = g.scale_rule;
     p.fast_math = g.fast_math;

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
                                                                    int* __restrict__ poff,
                                                                    int* __restrict__ chunk_base,
                                                                    int* __restrict__ block_expert,
+                                                                   int* __restrict__ block_rows,
                                                                    int* __restrict__ n_blocks) {
     __shared__ int s_warp[32];
     const int e = threadIdx.x;
@@ -123,7 +124,10 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
             *n_blocks = inc_p / kBlockM;
         }
         const int b0 = (inc_p - padded) / kBlockM;
-        for (int b = 0; b < padded / kBlockM; ++b) block_expert[b0 + b] = e;
+        for (int b = 0; b < padded / kBlockM; ++b) {
+            block_expert[b0 + b] = e;
+            if (block_rows) block_rows[b0 + b] = min(kBlockM, c_e - b * kBlockM);
+        }
     }
 }
 
@@ -202,6 +206,7 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
     }
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, L.chunks, L.E, count, off, poff, chunk_base,
                                                  reinterpret_cast<int*>(ws + L.block_expert),
+                                                 reinterpret_cast<int*>(ws + L.block_rows),
                                                  reinterpret_cast<int*>(ws + L.n_blocks));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     if (L.chunks > 0) {
@@ -278,7 +283,7 @@ extern "C" int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, 
         if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     }
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(scratch + kStaticHist, chunks, E, count, offsets, padded_offsets,
-                                                 scratch + kStaticBase, scratch + kStaticBlocks,
+                                                 scratch + kStaticBase, scratch + kStaticBlocks, nullptr,
                                                  scratch + kStaticNBlocks);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
