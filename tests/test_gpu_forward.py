@@ -111,3 +111,29 @@ def test_odd_h_tail_tile(moe, oracle):
     assert moe.plan_check(p) == 0
     ref = gh.oracle_forward(oracle, gh.host(d), w.E)
     gh.assert_close_output(gh.bits(y), ref["y"], "oddH")
+
+
+def test_largest_expert_count_and_topk(moe, oracle):
+    """E = 1024 experts and k = 32 (the library's limits): most experts get one
+    or two rows, so nearly every pool block is a 16-row-A block, and combine
+    sums 32 entries per token."""
+    w = inputs.Workload("maxEk", 64, 256, 128, 1024, 32, "uniform")
+    d, W1, W2 = gh.setup(moe, w)
+    p, y = run(moe, w, d, W1, W2)
+    assert moe.plan_check(p) == 0
+    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
+    gh.assert_close_output(gh.bits(y), ref["y"], "E=1024 k=32")
+
+
+def test_block_with_exactly_sixteen_and_seventeen_rows(moe, oracle):
+    """The 16-row A box is taken for blocks of at most 16 valid rows; 16 and 17
+    rows sit on both sides of that switch (and 144 = 128 + 16 on a second block)."""
+    w = inputs.Workload("edge16", 256, 256, 128, 4, 1, "uniform")
+    flat = np.concatenate([np.full(16, 0), np.full(17, 1), np.full(144, 2), np.full(79, 3)])
+    idx = np.random.default_rng(5).permutation(flat).reshape(w.T, 1)
+    tw = np.full((w.T, 1), 0.5, np.float32)
+    d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
+    p, y = run(moe, w, d, W1, W2)
+    assert moe.plan_check(p) == 0
+    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
+    gh.assert_close_output(gh.bits(y), ref["y"], "16/17 rows")
