@@ -50,11 +50,19 @@ constexpr int kBTxBytes = kBN * kBlockK / 2;   // a FP4 box's transaction count 
 // and two scale copies (SFA chunk, SFB chunk pair).
 constexpr int kStageSfOff = kABytes + kBBytes;   // SFA 512 B, then SFB pair 1 KB
 constexpr int kStageTxBytes = kABytes + kBTxBytes + 3 * kSfChunkBytes;
-// A row block with at most kSmallRows valid rows (decode-sized batches) loads
-// only those rows of A: the MMA still multiplies 128 rows, the others hold
-// stale shared memory and their accumulator rows are never stored.
-constexpr int kSmallRows = 16;
-constexpr int kSmallTxBytes = kStageTxBytes - (kBlockM - kSmallRows) * kBlockK;
+// A row block that is not full (an expert's last block, or decode-sized
+// batches) loads only the first 16, 32 or 64 rows of A that hold its valid
+// rows: the MMA still multiplies 128 rows, the others hold stale shared memory
+// and their accumulator rows are never stored.
+constexpr int kABoxLevels = 4;  // A boxes of 16, 32, 64 and 128 rows
+
+struct AMaps {
+    CUtensorMap box[kABoxLevels];
+};
+
+__device__ __forceinline__ int a_box_level(int rows) {
+    return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3;
+}
 constexpr int kStageStride = kABytes + kBBytes + 2048;  // 50 KB, a multiple of 1024
 constexpr int kBarrierBytes = 256;
 constexpr int kSmemBytes = kStages * kStageStride + kBarrierBytes + 1024;
@@ -257,8 +265,8 @@ __device__ __forceinline__ void store_tile_row(const GemmParams& p, int b, int j
 
 template <int kLayer>
 __global__ void __launch_bounds__(kThreads, 1)
-    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_a_small,
-                       const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    expert_gemm_kernel(const __grid_constant__ AMaps tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                       const GemmParams p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -281,8 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
         sh->abort = 0;
         ptx::fence_mbar_init();
-        ptx::prefetch_tensormap(&tmap_a);
-        ptx::prefetch_tensormap(&tmap_a_small);
+        for (int i = 0; i < kABoxLevels; ++i) ptx::prefetch_tensormap(&tmap_a.box[i]);
         ptx::prefetch_tensormap(&tmap_b);
     }
     if (warp == 1) {
@@ -319,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b_z = kLayer == 1 ? 2 * e : 0;
             const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
             const uint8_t* sfb = p.sfb + (static_cast<size_t>(e) * pairs + j) * kb_count * 2 * kSfChunkBytes;
-            const bool small = rows <= kSmallRows;  // valid rows of the block
+            const int level = a_box_level(rows);  // the A box that covers the block's valid rows
+            const uint32_t tx = kStageTxBytes - (kBlockM - (16 << level)) * kBlockK;
             for (int kb = 0; kb < kb_count; ++kb) {
                 if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
                     ok = false;
@@ -327,9 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 uint8_t* st = smem + stage * kStageStride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
-                ptx::mbar_arrive_expect_tx(full, small ? kSmallTxBytes : kStageTxBytes);
-                ptx::tma_load_2d(ptx::smem_addr(st), small ? &tmap_a_small : &tmap_a, kb * kBlockK, b * kBlockM,
-                                 full);
+                ptx::mbar_arrive_expect_tx(full, tx);
+                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a.box[level], kb * kBlockK, b * kBlockM, full);
                 if (kLayer == 1)
                     ptx::tma_load_3d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, b_z, full);
                 else
@@ -548,10 +555,11 @@ namespace {
 // map brings the gate and up rows for layer 1, a 256-row box for layer 2).
 cudaError_t launch_gemm(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
                           int num_sms, cudaStream_t s) {
-    CUtensorMap map_a, map_b;
-    CUtensorMap map_a_small;
-    bool maps_ok = make_map(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, kBlockM) &&
-                   make_map(&map_a_small, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, kSmallRows);
+    CUtensorMap map_b;
+    AMaps amaps;
+    bool maps_ok = true;
+    for (int i = 0; i < kABoxLevels; ++i)
+        maps_ok = maps_ok && make_map(&amaps.box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, 16u << i);
     if (layer == 1)  // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
         maps_ok = maps_ok && make_map_3d_fp4(&map_b, g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
     else
@@ -561,10 +569,10 @@ cudaError_t launch_gemm(int layer, const Layout& L, const GemmLaunch& g, const v
     cudaError_t st;
     if (layer == 1) {
         if ((st = smem_attr_once(expert_gemm_kernel<1>, 0, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_a_small, map_b, p);
+        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(amaps, map_b, p);
     } else {
         if ((st = smem_attr_once(expert_gemm_kernel<2>, 1, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(map_a, map_a_small, map_b, p);
+        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(amaps, map_b, p);
     }
     return cudaGetLastError();
 }

@@ -125,15 +125,17 @@ def test_largest_expert_count_and_topk(moe, oracle):
     gh.assert_close_output(gh.bits(y), ref["y"], "E=1024 k=32")
 
 
-def test_block_with_exactly_sixteen_and_seventeen_rows(moe, oracle):
-    """The 16-row A box is taken for blocks of at most 16 valid rows; 16 and 17
-    rows sit on both sides of that switch (and 144 = 128 + 16 on a second block)."""
-    w = inputs.Workload("edge16", 256, 256, 128, 4, 1, "uniform")
-    flat = np.concatenate([np.full(16, 0), np.full(17, 1), np.full(144, 2), np.full(79, 3)])
+def test_partial_blocks_on_every_a_box_size(moe, oracle):
+    """A block loads the smallest A box (16, 32, 64 or 128 rows) that holds its
+    valid rows; counts on both sides of each switch, and 144 = 128 + 16 for a
+    second block."""
+    counts = {0: 16, 1: 17, 2: 32, 3: 33, 4: 64, 5: 65, 6: 144, 7: 100}
+    flat = np.concatenate([np.full(n, e) for e, n in counts.items()])
+    w = inputs.Workload("boxes", flat.size, 256, 128, len(counts), 1, "uniform")
     idx = np.random.default_rng(5).permutation(flat).reshape(w.T, 1)
     tw = np.full((w.T, 1), 0.5, np.float32)
     d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
     ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], "16/17 rows")
+    gh.assert_close_output(gh.bits(y), ref["y"], "partial blocks")
