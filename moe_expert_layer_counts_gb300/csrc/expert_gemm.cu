@@ -15,7 +15,10 @@
 //   h = (g / (1 + exp(-g))) * u * topk_weight in fp32, requantised per 32 to
 //   E4M3 + UE8M0 (scales written in the tensor-core layout L2 reads).
 // Layer 2: a work item is (pool row block b, output tile j of 256 columns);
-//   epilogue rounds the fp32 accumulators to bf16 rows in pool order.
+//   epilogue rounds the fp32 accumulators to bf16 rows in pool order.  Each
+//   epilogue warp stages 32 rows x 32 columns at a time in shared memory and
+//   writes them with a TMA tensor store: per-thread row stores (32 rows x 16
+//   bytes per instruction) held up the next tile's operand loads.
 //
 // Warp roles (352 threads, one CTA per SM, persistent over work items):
 //   warp 0   TMA producer: A box, the B tile, the two scale copies per stage
@@ -56,22 +59,25 @@ constexpr int kStageTxBytes = kABytes + kBTxBytes + 3 * kSfChunkBytes;
 // and their accumulator rows are never stored.
 constexpr int kABoxLevels = 4;  // A boxes of 16, 32, 64 and 128 rows
 
-struct AMaps {
-    CUtensorMap box[kABoxLevels];
+struct Maps {
+    CUtensorMap box[kABoxLevels];  // A: boxes of 16, 32, 64 and 128 rows
+    CUtensorMap out;               // layer 2 output: bf16 [P_cap][H], box 32 x 32, 64-byte swizzle
 };
 
 __device__ __forceinline__ int a_box_level(int rows) {
     return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3;
 }
 constexpr int kStageStride = kABytes + kBBytes + 2048;  // 50 KB, a multiple of 1024
-constexpr int kBarrierBytes = 256;
-constexpr int kSmemBytes = kStages * kStageStride + kBarrierBytes + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+constexpr int kBarrierBytes = 1024;            // keeps the staging area 1024-byte aligned
+constexpr int kOutStageBytes = 2048;           // layer 2: 32 rows x 32 bf16 per epilogue warp
+constexpr int kOutStageOff = kStages * kStageStride + kBarrierBytes;
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemCol = 256;                // scale slots: 16 columns per stage
 constexpr int kThreads = 352;                  // 11 warps: TMA, MMA, 8 epilogue, scale copies
 constexpr int kEpiWarps = 8;
 constexpr int kScaleWarp = 10;
+constexpr int kSmemBytes = kOutStageOff + kEpiWarps * kOutStageBytes + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr uint64_t kWaitNs = 1000000000ull;    // 1 s per wait
 
 struct GemmParams {
@@ -239,33 +245,59 @@ __device__ __forceinline__ void drain_accumulator(uint32_t t_row, int half, uint
     }
 }
 
-// Store one pool row's share of a finished tile: layer 1 requantises 64
-// intermediate columns (two 32-blocks) to E4M3 + scales, layer 2 writes 128
-// bf16 output columns (clipped at H).
-template <int kLayer>
-__device__ __forceinline__ void store_tile_row(const GemmParams& p, int b, int j, int r, int quad, int half, int lane,
-                                               float wgt, const uint32_t (&pk)[64]) {
-    if (kLayer == 1) {
-        // intermediate columns j*128 + 64*half + [0, 64): two 32-blocks
-        uint8_t* dst = p.out_q + static_cast<size_t>(r) * p.I + j * 128 + 64 * half;
-        const uint32_t s0 = requant_block(pk, wgt, dst, p.clamp, p.scale_rule, p.fast_math);
-        const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32, p.clamp, p.scale_rule, p.fast_math);
-        const size_t chunk = static_cast<size_t>(b) * (p.I / 128) + j;
-        *reinterpret_cast<uint16_t*>(p.out_sf + chunk * kSfChunkBytes + 16 * lane + 4 * quad + 2 * half) =
-            static_cast<uint16_t>(s0 | (s1 << 8));
-    } else {
-        const int col0 = j * kBN + 128 * half;
-        const int ncol = p.H - col0;
-        uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + static_cast<size_t>(r) * p.H + col0);
+// Layer 1: requantise one pool row's 64 intermediate columns of a finished
+// tile (columns j*128 + 64*half + [0, 64), two 32-blocks) to E4M3 + scales.
+__device__ __forceinline__ void store_h_row(const GemmParams& p, int b, int j, int r, int quad, int half, int lane,
+                                            float wgt, const uint32_t (&pk)[64]) {
+    uint8_t* dst = p.out_q + static_cast<size_t>(r) * p.I + j * 128 + 64 * half;
+    const uint32_t s0 = requant_block(pk, wgt, dst, p.clamp, p.scale_rule, p.fast_math);
+    const uint32_t s1 = requant_block(pk + 32, wgt, dst + 32, p.clamp, p.scale_rule, p.fast_math);
+    const size_t chunk = static_cast<size_t>(b) * (p.I / 128) + j;
+    *reinterpret_cast<uint16_t*>(p.out_sf + chunk * kSfChunkBytes + 16 * lane + 4 * quad + 2 * half) =
+        static_cast<uint16_t>(s0 | (s1 << 8));
+}
+
+// Layer 2, partly filled row groups (an expert's last block; decode-sized
+// batches): each routed row's 128 bf16 columns straight from its lane.
+__device__ __forceinline__ void store_out_rows_direct(const GemmParams& p, int r, int col0, const uint32_t (&pk)[64]) {
+    uint4* dst = reinterpret_cast<uint4*>(p.out_bf16 + static_cast<size_t>(r) * p.H + col0);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (8 * i < ncol) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    for (int i = 0; i < 16; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+// Layer 2: one warp's 32 rows x 128 bf16 columns of a finished tile (lane =
+// row, columns col0 + [0, 128)) go out in four 32 x 32 blocks through the
+// warp's 2 KB staging buffer and a TMA tensor store each.  The buffer uses the
+// map's 64-byte swizzle (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)),
+// which also makes the row-per-lane writes free of bank conflicts.  Before a
+// buffer is rewritten, lane 0 waits until its previous store has read it.
+// Used when all 32 rows hold routed entries; a warp with padding rows writes
+// its routed rows directly (store_out_rows_direct).
+__device__ __forceinline__ void store_out_rows(const CUtensorMap* map, uint8_t* stg, int col0, int row0, int lane,
+                                               const uint32_t (&pk)[64]) {
+    const uint32_t stg_addr = ptx::smem_addr(stg);
+    const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t* v = pk + 16 * blk + 4 * c;
+            *reinterpret_cast<uint4*>(stg + lane * 64 + 16 * (c ^ sw)) = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            ptx::tma_store_2d(map, col0 + 32 * blk, row0, stg_addr);
+            ptx::bulk_commit_group();
+        }
     }
 }
 
 template <int kLayer>
 __global__ void __launch_bounds__(kThreads, 1)
-    expert_gemm_kernel(const __grid_constant__ AMaps tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+    expert_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ CUtensorMap tmap_b,
                        const GemmParams p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
     extern __shared__ uint8_t smem_raw[];
@@ -289,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
         sh->abort = 0;
         ptx::fence_mbar_init();
-        for (int i = 0; i < kABoxLevels; ++i) ptx::prefetch_tensormap(&tmap_a.box[i]);
+        for (int i = 0; i < kABoxLevels; ++i) ptx::prefetch_tensormap(&maps.box[i]);
         ptx::prefetch_tensormap(&tmap_b);
+        if (kLayer == 2) ptx::prefetch_tensormap(&maps.out);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&sh->tmem_base), kTmemCols);
@@ -336,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* st = smem + stage * kStageStride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
                 ptx::mbar_arrive_expect_tx(full, tx);
-                ptx::tma_load_2d(ptx::smem_addr(st), &tmap_a.box[level], kb * kBlockK, b * kBlockM, full);
+                ptx::tma_load_2d(ptx::smem_addr(st), &maps.box[level], kb * kBlockK, b * kBlockM, full);
                 if (kLayer == 1)
                     ptx::tma_load_3d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, b_z, full);
                 else
@@ -468,9 +501,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             drain_accumulator<kLayer>(t_row, half, pk, [&] {
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
             });
-            if (tok >= 0) store_tile_row<kLayer>(p, b, j, r, quad, half, lane, wgt, pk);
+            if (kLayer == 1) {
+                if (tok >= 0) store_h_row(p, b, j, r, quad, half, lane, wgt, pk);
+            } else {
+                const int col0 = j * kBN + 128 * half;  // H is a multiple of 128: a half is all in or all out
+                const uint32_t routed = __ballot_sync(0xffffffffu, tok >= 0);
+                if (col0 < p.H) {
+                    if (routed == 0xffffffffu)
+                        store_out_rows(&maps.out, smem + kOutStageOff + (warp - 2) * kOutStageBytes, col0,
+                                       b * kBlockM + quad * 32, lane, pk);
+                    else if (tok >= 0)
+                        store_out_rows_direct(p, r, col0, pk);
+                }
+            }
             acc_phase ^= 1;
         }
+        // this warp's tensor stores complete before the CTA exits
+        if (kLayer == 2 && lane == 0) ptx::bulk_wait_all();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -530,6 +577,20 @@ bool make_map_3d_fp4(CUtensorMap* map, const void* base, uint64_t k_elems, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [rows][cols] output map for tensor stores: box 32 columns x 32 rows,
+// 64-byte swizzle (the staging layout of store_out_rows).
+bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace {
@@ -556,10 +617,14 @@ namespace {
 cudaError_t launch_gemm(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
                           int num_sms, cudaStream_t s) {
     CUtensorMap map_b;
-    AMaps amaps;
+    Maps maps;
     bool maps_ok = true;
     for (int i = 0; i < kABoxLevels; ++i)
-        maps_ok = maps_ok && make_map(&amaps.box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, 16u << i);
+        maps_ok = maps_ok && make_map(&maps.box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, 16u << i);
+    if (layer == 2)
+        maps_ok = maps_ok && make_out_map(&maps.out, p.out_bf16, L.H, L.p_cap);
+    else
+        maps.out = maps.box[0];  // unused by layer 1
     if (layer == 1)  // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
         maps_ok = maps_ok && make_map_3d_fp4(&map_b, g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
     else
@@ -569,10 +634,10 @@ cudaError_t launch_gemm(int layer, const Layout& L, const GemmLaunch& g, const v
     cudaError_t st;
     if (layer == 1) {
         if ((st = smem_attr_once(expert_gemm_kernel<1>, 0, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(amaps, map_b, p);
+        expert_gemm_kernel<1><<<num_sms, kThreads, kSmemBytes, s>>>(maps, map_b, p);
     } else {
         if ((st = smem_attr_once(expert_gemm_kernel<2>, 1, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(amaps, map_b, p);
+        expert_gemm_kernel<2><<<num_sms, kThreads, kSmemBytes, s>>>(maps, map_b, p);
     }
     return cudaGetLastError();
 }
