@@ -212,7 +212,8 @@ enum {
     MOE_EXPORT_H_SF = 12,        /* uint8 [P_cap/128][I/128][512] UE8M0, tensor-core layout */
     MOE_EXPORT_L2_OUT = 13,      /* bf16 [P_cap, H] L2 output rows in pool order */
     MOE_EXPORT_ERROR = 14,       /* int32 [2] device error record: bits, then where a wait expired */
-    MOE_EXPORT_POOL_ROWS = 15    /* (size only) P_cap, the pool row capacity, in the size field */
+    MOE_EXPORT_POOL_ROWS = 15,   /* (size only) P_cap, the pool row capacity, in the size field */
+    MOE_EXPORT_MAX_COUNT = 16    /* int32 [1] largest expert count (0 when nothing is routed) */
 };
 int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* bytes);
 

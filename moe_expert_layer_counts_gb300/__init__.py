@@ -37,11 +37,13 @@ SF_PAIRS_ADJACENT = 0
 SF_PAIRS_HALVES = 1
 
 EXPORT = dict(count=0, off=1, poff=2, slot_of=3, row_token=4, row_topk=5, row_weight=6, block_expert=7,
-              n_blocks=8, pool_q=9, pool_sf=10, h_q=11, h_sf=12, l2_out=13, error=14, pool_rows=15)
+              n_blocks=8, pool_q=9, pool_sf=10, h_q=11, h_sf=12, l2_out=13, error=14, pool_rows=15,
+              max_count=16)
 _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_of=torch.int32,
                      row_token=torch.int32, row_topk=torch.int32, row_weight=torch.float32,
                      block_expert=torch.int32, n_blocks=torch.int32, pool_q=torch.uint8, pool_sf=torch.uint8,
-                     h_q=torch.uint8, h_sf=torch.uint8, l2_out=torch.bfloat16, error=torch.int32)
+                     h_q=torch.uint8, h_sf=torch.uint8, l2_out=torch.bfloat16, error=torch.int32,
+                     max_count=torch.int32)
 
 # every function declared in include/moe.h
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",

@@ -129,6 +129,7 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
     };
     L->err = take(2 * sizeof(int));
     L->n_blocks = take(sizeof(int));
+    L->max_count = take(sizeof(int));  // largest expert count (selects the GEMM's operand ring)
     L->count = take(sizeof(int) * E);
     L->off = take(sizeof(int) * (E + 1));
     L->poff = take(sizeof(int) * (E + 1));
@@ -311,6 +312,7 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
         case MOE_EXPORT_L2_OUT: *offset = L.l2_out; *bytes = cap * ps->H * 2; break;
         case MOE_EXPORT_ERROR: *offset = L.err; *bytes = 8; break;
         case MOE_EXPORT_POOL_ROWS: *offset = 0; *bytes = cap; break;
+        case MOE_EXPORT_MAX_COUNT: *offset = L.max_count; *bytes = 4; break;
         default: return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;

@@ -43,16 +43,30 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kBN = 256;                       // MMA N: 256 weight rows (gate|up halves for layer 1)
 constexpr int kABytes = kBlockM * kBlockK;     // 16 KB of E4M3
 constexpr int kBBytes = kBN * kBlockK;         // 32 KB in smem: E2M1 unpacked to one byte per element
 constexpr int kBTxBytes = kBN * kBlockK / 2;   // a FP4 box's transaction count is its packed size
-// A stage: A box (16 KB), the whole B tile in one request (a 3-D map for
-// layer 1 brings the gate and up rows together; a 256-row box for layer 2),
-// and two scale copies (SFA chunk, SFB chunk pair).
-constexpr int kStageSfOff = kABytes + kBBytes;   // SFA 512 B, then SFB pair 1 KB
+// A stage: the A box, the whole B tile in one request (a 3-D map for layer 1
+// brings the gate and up rows together; a 256-row box for layer 2), and two
+// scale copies (SFA chunk 512 B, SFB chunk pair 1 KB) after A and B.
 constexpr int kStageTxBytes = kABytes + kBTxBytes + 3 * kSfChunkBytes;
+// The operand ring has one of two shapes, chosen per launch from the plan:
+//   wide:   4 stages of 50 KB (A 16 KB for 128 rows, B 32 KB, scales 2 KB)
+//   narrow: 6 stages of 36 KB (A 2 KB for 16 rows, B, scales), used when no
+//           expert has more than 16 rows (decode-sized batches): the stream is
+//           then weight bytes from HBM, and 6 stages keep 50% more of them in
+//           flight.  The MMA still reads a 16 KB A window from the stage start;
+//           beyond the 16 loaded rows it covers the stage's own B bytes, which
+//           feed only accumulator rows that are never stored.
+constexpr int kMaxStages = 6;
+constexpr int kWideStages = 4, kWideStride = 51200, kWideABytes = kABytes;
+constexpr int kNarrowStages = 6, kNarrowStride = 36864, kNarrowABytes = 16 * kBlockK;
+constexpr int kNarrowRows = 16;
+static_assert(kWideABytes + kBBytes + 3 * kSfChunkBytes <= kWideStride && kWideStride % 1024 == 0, "wide stage");
+static_assert(kNarrowABytes + kBBytes + 3 * kSfChunkBytes <= kNarrowStride && kNarrowStride % 1024 == 0,
+              "narrow stage");
+static_assert(kNarrowABytes + kBBytes >= kABytes, "the MMA's A window stays inside a narrow stage");
 // A row block that is not full (an expert's last block, or decode-sized
 // batches) loads only the first 16, 32 or 64 rows of A that hold its valid
 // rows: the MMA still multiplies 128 rows, the others hold stale shared memory
@@ -67,17 +81,22 @@ struct Maps {
 __device__ __forceinline__ int a_box_level(int rows) {
     return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3;
 }
-constexpr int kStageStride = kABytes + kBBytes + 2048;  // 50 KB, a multiple of 1024
-constexpr int kBarrierBytes = 1024;            // keeps the staging area 1024-byte aligned
+// Shared memory: barriers (1 KB), the ring, and (wide ring only) the layer-2
+// output staging, which a narrow ring overlaps: with at most 16 rows per
+// block no epilogue warp ever holds 32 routed rows, the staged path's condition.
+constexpr int kRingOff = 1024;
 constexpr int kOutStageBytes = 2048;           // layer 2: 32 rows x 32 bf16 per epilogue warp
-constexpr int kOutStageOff = kStages * kStageStride + kBarrierBytes;
+constexpr int kOutStageOff = kRingOff + kWideStages * kWideStride;
 constexpr int kTmemCols = 512;
 constexpr int kSfTmemCol = 256;                // scale slots: 16 columns per stage
 constexpr int kThreads = 352;                  // 11 warps: TMA, MMA, 8 epilogue, scale copies
 constexpr int kEpiWarps = 8;
 constexpr int kScaleWarp = 10;
-constexpr int kSmemBytes = kOutStageOff + kEpiWarps * kOutStageBytes + 1024;
+constexpr int kSmemEnd = kOutStageOff + kEpiWarps * kOutStageBytes;
+static_assert(kRingOff + kNarrowStages * kNarrowStride <= kSmemEnd, "narrow ring inside the allocation");
+constexpr int kSmemBytes = kSmemEnd + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSfTmemCol + 16 * kMaxStages <= kTmemCols, "scale slots");
 constexpr uint64_t kWaitNs = 1000000000ull;    // 1 s per wait
 
 struct GemmParams {
@@ -100,12 +119,13 @@ struct GemmParams {
     int scale_rule;         // layer 1: 0 = ceil, 1 = OCP floor (scales of h)
     int fast_math;          // layer 1: 0 = every SwiGLU value by the exact formula
     const int* block_rows;  // valid rows of each pool row block (plan)
+    const int* max_count;   // largest expert count (plan): selects the ring shape
 };
 
 struct Shared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t sf_ready[kStages];   // the stage's scales are in tensor memory
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t sf_ready[kMaxStages];   // the stage's scales are in tensor memory
     uint64_t sf_drain;
     uint64_t tmem_full;
     uint64_t tmem_empty;
@@ -302,15 +322,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared* sh = reinterpret_cast<Shared*>(smem + kStages * kStageStride);
+    Shared* sh = reinterpret_cast<Shared*>(smem);
+    uint8_t* ring = smem + kRingOff;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int n_work = *p.n_blocks * p.n_tiles;
     if (static_cast<int>(blockIdx.x) >= n_work) return;  // uniform for the CTA
     const int kb_count = p.K / kBlockK;
+    // ring shape (uniform for the launch)
+    const bool narrow = *p.max_count <= kNarrowRows;
+    const int n_stages = narrow ? kNarrowStages : kWideStages;
+    const int stride = narrow ? kNarrowStride : kWideStride;
+    const int a_bytes = narrow ? kNarrowABytes : kWideABytes;
+    const int sf_off = a_bytes + kBBytes;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kMaxStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(&sh->full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh->empty[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh->sf_ready[s]), 1);
@@ -366,20 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                uint8_t* st = smem + stage * kStageStride;
+                uint8_t* st = ring + stage * stride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
                 ptx::mbar_arrive_expect_tx(full, tx);
                 ptx::tma_load_2d(ptx::smem_addr(st), &maps.box[level], kb * kBlockK, b * kBlockM, full);
                 if (kLayer == 1)
-                    ptx::tma_load_3d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, b_z, full);
+                    ptx::tma_load_3d(ptx::smem_addr(st + a_bytes), &tmap_b, kb * kBlockK, b_y, b_z, full);
                 else
-                    ptx::tma_load_2d(ptx::smem_addr(st + kABytes), &tmap_b, kb * kBlockK, b_y, full);
-                ptx::bulk_load(ptx::smem_addr(st + kStageSfOff), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
-                ptx::bulk_load(ptx::smem_addr(st + kStageSfOff + kSfChunkBytes), sfb + kb * 2 * kSfChunkBytes,
+                    ptx::tma_load_2d(ptx::smem_addr(st + a_bytes), &tmap_b, kb * kBlockK, b_y, full);
+                ptx::bulk_load(ptx::smem_addr(st + sf_off), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
+                ptx::bulk_load(ptx::smem_addr(st + sf_off + kSfChunkBytes), sfb + kb * 2 * kSfChunkBytes,
                                2 * kSfChunkBytes, full);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == kStages) {
+                if (++stage == n_stages) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -387,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) {
             // let this CTA's copies in flight land before the CTA may exit
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < n_stages; ++s)
                 if (issued_mask & (1u << s))
                     ptx::mbar_wait(ptx::smem_addr(&sh->full[s]), (issued_parity >> s) & 1u,
                                    ptx::globaltimer() + kWaitNs);
@@ -402,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage 0 plus the stage offset in 16-byte units (the start-address
         // field); a 32-wide K step adds 2.
         constexpr uint32_t idesc = ptx::idesc_e4m3_e2m1(kBlockM, kBN);
-        const uint32_t st0 = ptx::smem_addr(smem);
+        const uint32_t st0 = ptx::smem_addr(ring);
         const uint64_t a_desc0 = ptx::desc_kmajor_sw128(st0);
-        const uint64_t b_desc0 = ptx::desc_kmajor_sw128(st0 + kABytes);
+        const uint64_t b_desc0 = ptx::desc_kmajor_sw128(st0 + a_bytes);
         const uint32_t ready0 = ptx::smem_addr(&sh->sf_ready[0]);
         const uint32_t empty0 = ptx::smem_addr(&sh->empty[0]);
         const uint32_t tsf0 = tmem + kSfTmemCol;
@@ -421,14 +448,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint64_t so = static_cast<uint64_t>(stage * (kStageStride >> 4));
+                const uint64_t so = static_cast<uint64_t>(stage * (stride >> 4));
                 const uint32_t tsf = tsf0 + 16 * stage;
 #pragma unroll
                 for (int kk = 0; kk < kBlockK / 32; ++kk)
                     ptx::mma_mxf8f6f4(tmem, a_desc0 + so + 2 * kk, b_desc0 + so + 2 * kk,
                                       ptx::idesc_with_sf_id(idesc, kk), tsf + 0, tsf + 4, (kb | kk) != 0);
                 ptx::tc_commit(empty0 + 8 * stage);
-                if (++stage == kStages) {
+                if (++stage == n_stages) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -449,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // waiting for them to complete.  The slot is free by then: the stage
         // was refilled only after the MMAs that last read the slot had
         // completed.
-        const uint64_t sf_desc0 = ptx::desc_sf_32x16(ptx::smem_addr(smem) + kStageSfOff);
+        const uint64_t sf_desc0 = ptx::desc_sf_32x16(ptx::smem_addr(ring) + sf_off);
         const uint32_t full0 = ptx::smem_addr(&sh->full[0]);
         const uint32_t ready0 = ptx::smem_addr(&sh->sf_ready[0]);
         const uint32_t tsf0 = tmem + kSfTmemCol;
@@ -463,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint64_t so = static_cast<uint64_t>(stage * (kStageStride >> 4));
+                const uint64_t so = static_cast<uint64_t>(stage * (stride >> 4));
                 const uint32_t tsf = tsf0 + 16 * stage;
                 ptx::tc_cp_32x128b_warpx4(tsf + 0, sf_desc0 + so);
                 ptx::tc_cp_32x128b_warpx4(tsf + 4, sf_desc0 + so + (kSfChunkBytes >> 4));
@@ -472,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // seen this arrive (and fenced) execute after these copies
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ready0 + 8 * stage);
-                if (++stage == kStages) {
+                if (++stage == n_stages) {
                     stage = 0;
                     phase ^= 1;
                 }
@@ -507,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col0 = j * kBN + 128 * half;  // H is a multiple of 128: a half is all in or all out
                 const uint32_t routed = __ballot_sync(0xffffffffu, tok >= 0);
                 if (col0 < p.H) {
-                    if (routed == 0xffffffffu)
+                    if (!narrow && routed == 0xffffffffu)
                         store_out_rows(&maps.out, smem + kOutStageOff + (warp - 2) * kOutStageBytes, col0,
                                        b * kBlockM + quad * 32, lane, pk);
                     else if (tok >= 0)
@@ -659,6 +686,7 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     p.H = L.H;
     p.err = reinterpret_cast<int*>(ws + L.err);
     p.block_rows = reinterpret_cast<const int*>(ws + L.block_rows);
+    p.max_count = reinterpret_cast<const int*>(ws + L.max_count);
     p.clamp = g.clamp > 0.0f ? g.clamp : std::numeric_limits<float>::infinity();  // no clamp
     p.scale_rule = g.scale_rule;
     p.fast_math = g.fast_math;

@@ -27,7 +27,7 @@ struct Layout {
     int T, k, E, H, I;
     int chunks;        // routing chunks (CTAs of the count / slot kernels)
     int64_t p_cap;     // pool row capacity (multiple of kBlockM)
-    size_t err, n_blocks, count, off, poff, hist, chunk_base, block_expert, block_rows;
+    size_t err, n_blocks, max_count, count, off, poff, hist, chunk_base, block_expert, block_rows;
     size_t slot_of, row_token, row_topk, row_weight;
     size_t pool_q, pool_sf, h_q, h_sf, l2_out;
     size_t total;

@@ -99,10 +99,14 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
                                                                    int* __restrict__ chunk_base,
                                                                    int* __restrict__ block_expert,
                                                                    int* __restrict__ block_rows,
-                                                                   int* __restrict__ n_blocks) {
+                                                                   int* __restrict__ n_blocks,
+                                                                   int* __restrict__ max_count) {
     __shared__ int s_warp[32];
+    __shared__ int s_max;
     const int e = threadIdx.x;
     int c_e = 0;
+    if (e == 0) s_max = 0;
+    __syncthreads();
     if (e < E) {
 #pragma unroll 8
         for (int c = 0; c < chunks; ++c) {
@@ -111,6 +115,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
             c_e += v;
         }
         count[e] = c_e;
+        if (max_count && c_e > 0) atomicMax(&s_max, c_e);
     }
     const int padded = (c_e + kBlockM - 1) / kBlockM * kBlockM;
     const int inc_c = block_inclusive_scan(c_e, s_warp);
@@ -123,6 +128,8 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
             poff[E] = inc_p;
             *n_blocks = inc_p / kBlockM;
         }
+        // s_max is final: the scans above passed block-wide barriers
+        if (e == 0 && max_count) *max_count = s_max;
         const int b0 = (inc_p - padded) / kBlockM;
         for (int b = 0; b < padded / kBlockM; ++b) {
             block_expert[b0 + b] = e;
@@ -207,7 +214,8 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, L.chunks, L.E, count, off, poff, chunk_base,
                                                  reinterpret_cast<int*>(ws + L.block_expert),
                                                  reinterpret_cast<int*>(ws + L.block_rows),
-                                                 reinterpret_cast<int*>(ws + L.n_blocks));
+                                                 reinterpret_cast<int*>(ws + L.n_blocks),
+                                                 reinterpret_cast<int*>(ws + L.max_count));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     if (L.chunks > 0) {
         const size_t smem = static_cast<size_t>(L.E) * (1 + kSlotWarps) * sizeof(int);
@@ -284,6 +292,6 @@ extern "C" int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, 
     }
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(scratch + kStaticHist, chunks, E, count, offsets, padded_offsets,
                                                  scratch + kStaticBase, scratch + kStaticBlocks, nullptr,
-                                                 scratch + kStaticNBlocks);
+                                                 scratch + kStaticNBlocks, nullptr);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

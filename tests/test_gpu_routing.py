@@ -28,6 +28,7 @@ def compare_plan(moe, oracle, idx, tw, E, H=256, I=128):
     np.testing.assert_array_equal(g("slot_of"), ref["slot_of"])
     P = int(ref["poff"][-1])
     assert int(g("n_blocks")[0]) == P // 128
+    assert int(g("max_count")[0]) == int(ref["count"].max(initial=0))
     np.testing.assert_array_equal(g("row_token")[:P], ref["row_token"][:P])
     np.testing.assert_array_equal(g("row_topk")[:P], ref["row_topk"][:P])
     np.testing.assert_array_equal(g("row_weight")[:P].view(np.uint32), ref["row_weight"][:P].view(np.uint32))
@@ -69,6 +70,7 @@ def test_empty_batch(moe):
     p, st = run_plan(moe, np.zeros((0, 4), np.int64), np.zeros((0, 4), np.float32), 8)
     assert st == 0
     assert int(p.export("n_blocks").cpu()[0]) == 0
+    assert int(p.export("max_count").cpu()[0]) == 0
     assert p.export("count").sum().item() == 0
 
 
