@@ -15,10 +15,11 @@
 //                per warp, via __match_any_sync)
 //   route_scan   one CTA: per-expert prefix over chunks, exclusive scans of
 //                counts and of counts padded to MOE_BLOCK_M, the row-block ->
-//                expert table and the number of row blocks
+//                expert table, the number of row blocks, and the inverse maps
+//                of the padding rows (one warp per expert)
 //   route_slot   one CTA per chunk: ranks inside the chunk in flat order
 //                (rank in warp from the match mask, plus same-expert counts of
-//                lower warps), inverse maps of every pool row, padding rows
+//                lower warps), inverse maps of every routed pool row
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -100,9 +101,13 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
                                                                    int* __restrict__ block_expert,
                                                                    int* __restrict__ block_rows,
                                                                    int* __restrict__ n_blocks,
-                                                                   int* __restrict__ max_count) {
+                                                                   int* __restrict__ max_count,
+                                                                   int* __restrict__ row_token,
+                                                                   int* __restrict__ row_topk,
+                                                                   float* __restrict__ row_weight) {
     __shared__ int s_warp[32];
     __shared__ int s_max;
+    __shared__ int s_pad[2][kScanThreads];  // padding rows [begin, end) of each expert
     const int e = threadIdx.x;
     int c_e = 0;
     if (e == 0) s_max = 0;
@@ -135,12 +140,25 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
             block_expert[b0 + b] = e;
             if (block_rows) block_rows[b0 + b] = min(kBlockM, c_e - b * kBlockM);
         }
+        s_pad[0][e] = inc_p - padded + c_e;
+        s_pad[1][e] = inc_p;
+    }
+    if (!row_token) return;  // uniform: the counts-only path has no pool
+    __syncthreads();
+    // padding rows (fewer than MOE_BLOCK_M per expert): one warp per expert
+    const int lane = threadIdx.x & 31;
+    for (int x = threadIdx.x >> 5; x < E; x += kScanThreads / 32) {
+        for (int r = s_pad[0][x] + lane; r < s_pad[1][x]; r += 32) {
+            row_token[r] = -1;
+            row_topk[r] = -1;
+            row_weight[r] = 0.0f;
+        }
     }
 }
 
 __global__ void __launch_bounds__(kSlotThreads) route_slot_kernel(
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
-    const int* __restrict__ count, const int* __restrict__ poff, const int* __restrict__ chunk_base,
+    const int* __restrict__ poff, const int* __restrict__ chunk_base,
     int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
     float* __restrict__ row_weight) {
     extern __shared__ int s_mem[];
@@ -183,15 +201,6 @@ __global__ void __launch_bounds__(kSlotThreads) route_slot_kernel(
             }
         }
     }
-    // padding rows of this CTA's share of experts
-    for (int e = blockIdx.x; e < E; e += gridDim.x) {
-        const int p0 = poff[e] + count[e], p1 = poff[e + 1];
-        for (int r = p0 + threadIdx.x; r < p1; r += blockDim.x) {
-            row_token[r] = -1;
-            row_topk[r] = -1;
-            row_weight[r] = 0.0f;
-        }
-    }
 }
 
 }  // namespace
@@ -215,12 +224,15 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
                                                  reinterpret_cast<int*>(ws + L.block_expert),
                                                  reinterpret_cast<int*>(ws + L.block_rows),
                                                  reinterpret_cast<int*>(ws + L.n_blocks),
-                                                 reinterpret_cast<int*>(ws + L.max_count));
+                                                 reinterpret_cast<int*>(ws + L.max_count),
+                                                 reinterpret_cast<int*>(ws + L.row_token),
+                                                 reinterpret_cast<int*>(ws + L.row_topk),
+                                                 reinterpret_cast<float*>(ws + L.row_weight));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     if (L.chunks > 0) {
         const size_t smem = static_cast<size_t>(L.E) * (1 + kSlotWarps) * sizeof(int);
         route_slot_kernel<<<L.chunks, kSlotThreads, smem, s>>>(
-            topk_idx, topk_w, n, L.k, L.E, count, poff, chunk_base, reinterpret_cast<int*>(ws + L.slot_of),
+            topk_idx, topk_w, n, L.k, L.E, poff, chunk_base, reinterpret_cast<int*>(ws + L.slot_of),
             reinterpret_cast<int*>(ws + L.row_token), reinterpret_cast<int*>(ws + L.row_topk),
             reinterpret_cast<float*>(ws + L.row_weight));
         if ((st = cudaGetLastError()) != cudaSuccess) return st;
@@ -292,6 +304,6 @@ extern "C" int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, 
     }
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(scratch + kStaticHist, chunks, E, count, offsets, padded_offsets,
                                                  scratch + kStaticBase, scratch + kStaticBlocks, nullptr,
-                                                 scratch + kStaticNBlocks, nullptr);
+                                                 scratch + kStaticNBlocks, nullptr, nullptr, nullptr, nullptr);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
