@@ -141,22 +141,24 @@ def test_partial_blocks_on_every_a_box_size(moe, oracle):
     gh.assert_close_output(gh.bits(y), ref["y"], "partial blocks")
 
 
-@pytest.mark.parametrize("largest", [16, 17])
-def test_ring_shape_switch(moe, oracle, largest):
+@pytest.mark.parametrize("largest,H", [(16, 1024), (17, 1024), (16, 384)])
+def test_ring_shape_switch(moe, oracle, largest, H):
     """With no expert above 16 rows the GEMMs run the 6-stage narrow ring
     (16-row A stages), otherwise the 4-stage wide ring: 200 experts of 1 to 16
     rows plus one of `largest`, H = 1024 (8 k-blocks per L1 tile) so that each
-    CTA's ring wraps several times over its tiles."""
+    CTA's ring wraps several times over its tiles; H = 384 adds a half-empty
+    last L2 output tile to the narrow ring."""
     rng = np.random.default_rng(11)
     counts = rng.integers(1, 17, size=200)
     counts[0] = 16
     counts[1] = largest
     flat = np.concatenate([np.full(n, e) for e, n in enumerate(counts)])
-    w = inputs.Workload("ring", flat.size, 1024, 256, counts.size, 1, "uniform")
+    w = inputs.Workload("ring", flat.size, H, 256, counts.size, 1, "uniform")
     idx = rng.permutation(flat).reshape(w.T, 1)
     tw = np.full((w.T, 1), 0.75, np.float32)
     d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
     ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], f"ring, largest count {largest}")
+    assert int(p.export("max_count").cpu()[0]) == largest
+    gh.assert_close_output(gh.bits(y), ref["y"], f"ring, largest count {largest}, H {H}")
