@@ -20,6 +20,9 @@
 //   route_slot   one CTA per chunk: ranks inside the chunk in flat order
 //                (rank in warp from the match mask, plus same-expert counts of
 //                lower warps), inverse maps of every routed pool row
+// A batch of at most kRouteChunk entries (decode-sized) takes one kernel
+// instead, route_small: the same three steps in one CTA, so the plan is a
+// single launch.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -31,6 +34,9 @@ constexpr int kCountThreads = 256;
 constexpr int kSlotThreads = 256;
 constexpr int kSlotWarps = kSlotThreads / 32;
 constexpr int kScanThreads = 1024;
+constexpr int kSmallThreads = 256;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallPerThread = (kMaxExperts + kSmallThreads - 1) / kSmallThreads;  // experts per thread
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -203,6 +209,127 @@ __global__ void __launch_bounds__(kSlotThreads) route_slot_kernel(
     }
 }
 
+// All of routing for n <= kRouteChunk entries in one CTA: counts (shared
+// histogram), exclusive scans of the counts and of the counts padded to
+// MOE_BLOCK_M (thread t owns experts [t*per, t*per + per)), the row-block
+// tables, the padding rows, then the stable slots exactly as route_slot ranks
+// them (chunk base 0).  Also zeroes the error record and sets the bad-id bit.
+__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
+    const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int n, int k, int E,
+    int* __restrict__ count, int* __restrict__ off, int* __restrict__ poff, int* __restrict__ block_expert,
+    int* __restrict__ block_rows, int* __restrict__ n_blocks, int* __restrict__ max_count, int* __restrict__ slot_of,
+    int* __restrict__ row_token, int* __restrict__ row_topk, float* __restrict__ row_weight, int* __restrict__ err) {
+    extern __shared__ int s_mem[];
+    int* s_cnt = s_mem;                      // [E] counts, later the next free slot of each expert
+    int* s_wcnt = s_mem + E;                 // [kSmallWarps][E] same-expert counts per warp, this round
+    int* s_pad = s_mem + E * (1 + kSmallWarps);  // [2][E] padding rows [begin, end) of each expert
+    __shared__ int s_warp[32];
+    __shared__ int s_max, s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += kSmallThreads) {
+        s_cnt[e] = 0;
+        for (int w = 0; w < kSmallWarps; ++w) s_wcnt[w * E + e] = 0;
+    }
+    if (tid == 0) {
+        s_max = 0;
+        s_bad = 0;
+    }
+    __syncthreads();
+    // 1. counts
+    bool bad = false;
+    for (int i0 = 0; i0 < n; i0 += kSmallThreads) {
+        const int e = entry_expert(topk_idx, i0 + tid, n, E, &bad);
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(same) - 1) atomicAdd(&s_cnt[e], __popc(same));
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+    // 2. scans over experts, per-thread runs of kSmallPerThread
+    const int per = (E + kSmallThreads - 1) / kSmallThreads;
+    int c[kSmallPerThread];
+    int sum_c = 0, sum_p = 0, mx = 0;
+#pragma unroll
+    for (int q = 0; q < kSmallPerThread; ++q) {
+        const int e = tid * per + q;
+        c[q] = (q < per && e < E) ? s_cnt[e] : 0;
+        sum_c += c[q];
+        sum_p += (c[q] + kBlockM - 1) / kBlockM * kBlockM;
+        mx = max(mx, c[q]);
+    }
+    if (mx > 0) atomicMax(&s_max, mx);
+    const int inc_c = block_inclusive_scan(sum_c, s_warp);
+    const int inc_p = block_inclusive_scan(sum_p, s_warp);
+    int o_c = inc_c - sum_c, o_p = inc_p - sum_p;
+#pragma unroll
+    for (int q = 0; q < kSmallPerThread; ++q) {
+        const int e = tid * per + q;
+        if (q < per && e < E) {
+            const int padded = (c[q] + kBlockM - 1) / kBlockM * kBlockM;
+            count[e] = c[q];
+            off[e] = o_c;
+            poff[e] = o_p;
+            for (int b = 0; b < padded / kBlockM; ++b) {
+                block_expert[o_p / kBlockM + b] = e;
+                block_rows[o_p / kBlockM + b] = min(kBlockM, c[q] - b * kBlockM);
+            }
+            s_pad[e] = o_p + c[q];
+            s_pad[E + e] = o_p + padded;
+            s_cnt[e] = o_p;  // next free slot (the chunk base is 0)
+            o_c += c[q];
+            o_p += padded;
+            if (e == E - 1) {
+                off[E] = o_c;
+                poff[E] = o_p;
+                *n_blocks = o_p / kBlockM;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        *max_count = s_max;
+        err[0] = s_bad ? kDevErrBadExpert : 0;
+        err[1] = 0;
+    }
+    // padding rows: one warp per expert
+    for (int x = warp; x < E; x += kSmallWarps) {
+        for (int r = s_pad[x] + lane; r < s_pad[E + x]; r += 32) {
+            row_token[r] = -1;
+            row_topk[r] = -1;
+            row_weight[r] = 0.0f;
+        }
+    }
+    // 3. stable slots, in rounds of kSmallThreads entries in flat order
+    for (int i0 = 0; i0 < n; i0 += kSmallThreads) {
+        const int i = i0 + tid;
+        bool unused = false;
+        const int e = entry_expert(topk_idx, i, n, E, &unused);
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        const bool leader = lane == __ffs(same) - 1;
+        if (e >= 0 && leader) s_wcnt[warp * E + e] = __popc(same);
+        __syncthreads();
+        int slot = -1;
+        if (e >= 0) {
+            int before = __popc(same & lanemask_lt());
+            for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
+            slot = s_cnt[e] + before;
+        }
+        __syncthreads();
+        if (e >= 0 && leader) {
+            atomicAdd(&s_cnt[e], __popc(same));
+            s_wcnt[warp * E + e] = 0;
+        }
+        __syncthreads();
+        if (i < n) {
+            slot_of[i] = slot;
+            if (slot >= 0) {
+                row_token[slot] = i / k;
+                row_topk[slot] = i % k;
+                row_weight[slot] = __ldg(topk_w + i);
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, const float* topk_w,
@@ -214,6 +341,16 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
     int* off = reinterpret_cast<int*>(ws + L.off);
     int* poff = reinterpret_cast<int*>(ws + L.poff);
     int* chunk_base = reinterpret_cast<int*>(ws + L.chunk_base);
+    if (L.chunks == 1) {  // one kernel for a decode-sized batch
+        const size_t smem = static_cast<size_t>(L.E) * (3 + kSmallWarps) * sizeof(int);
+        route_small_kernel<<<1, kSmallThreads, smem, s>>>(
+            topk_idx, topk_w, static_cast<int>(n), L.k, L.E, count, off, poff,
+            reinterpret_cast<int*>(ws + L.block_expert), reinterpret_cast<int*>(ws + L.block_rows),
+            reinterpret_cast<int*>(ws + L.n_blocks), reinterpret_cast<int*>(ws + L.max_count),
+            reinterpret_cast<int*>(ws + L.slot_of), reinterpret_cast<int*>(ws + L.row_token),
+            reinterpret_cast<int*>(ws + L.row_topk), reinterpret_cast<float*>(ws + L.row_weight), err);
+        return cudaGetLastError();
+    }
     cudaError_t st = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
     if (st != cudaSuccess) return st;
     if (L.chunks > 0) {

@@ -66,6 +66,18 @@ def test_plan_edge_cases(moe, oracle):
     compare_plan(moe, oracle, idx, rng.random((100, 4)), 8)
 
 
+@pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096])
+def test_plan_one_kernel_and_chunked_paths(moe, oracle, n):
+    """Up to 2048 entries the plan is one single-CTA kernel, above it the
+    chunked count / scan / slot kernels: both sides of the switch, with
+    skipped and bad ids and 1024 experts."""
+    rng = np.random.default_rng(n)
+    idx = rng.integers(-1, 1024, size=(n, 1))
+    if n > 3:
+        idx[n // 2, 0] = 1024
+    compare_plan(moe, oracle, idx, rng.random((n, 1)), 1024)
+
+
 def test_empty_batch(moe):
     p, st = run_plan(moe, np.zeros((0, 4), np.int64), np.zeros((0, 4), np.float32), 8)
     assert st == 0
