@@ -159,8 +159,8 @@ def cpu_baseline(w, d, target_s: float):
     oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
     t_cal = time.perf_counter() - t0
     n, dt = len(toks), t_cal
-    for _ in range(2):  # the time grows less than linearly (per-expert weight decoding), so refine once
-        if n >= w.T or dt >= 0.5 * target_s:
+    for _ in range(3):  # the time grows less than linearly (per-expert weight decoding): refine from the last run
+        if n >= w.T or dt >= 0.7 * target_s:
             break
         n = int(min(w.T, max(n + 1, n * target_s / max(dt, 1e-6))))
         step, toks = sample(n)
@@ -217,7 +217,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="full", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU time the cpu_baseline sample aims at")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU time the cpu_baseline sample aims at")
     ap.add_argument("--ref-tokens", type=int, default=1, help="oracle tokens per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
