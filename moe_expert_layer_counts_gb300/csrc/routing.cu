@@ -34,9 +34,18 @@ constexpr int kCountThreads = 256;
 constexpr int kSlotThreads = 256;
 constexpr int kSlotWarps = kSlotThreads / 32;
 constexpr int kScanThreads = 1024;
-constexpr int kSmallThreads = 256;
-constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallPerThread = (kMaxExperts + kSmallThreads - 1) / kSmallThreads;  // experts per thread
+// route_small runs as many warps (up to 32) as keep its shared memory, E x
+// (3 + warps) ints, within 47 KB (under the 48 KB default): 32 warps up to E = 343, 8 at
+// E = 1024.
+constexpr int kSmallMaxThreads = 1024;
+constexpr int kSmallMinThreads = 256;
+constexpr int kSmallSmemInts = 47 * 1024 / 4;  // leaves room for the static shared arrays
+constexpr int kSmallPerThread = (kMaxExperts + kSmallMinThreads - 1) / kSmallMinThreads;  // experts per thread
+__host__ __device__ constexpr int small_threads(int E) {
+    return E * (3 + kSmallMaxThreads / 32) <= kSmallSmemInts
+               ? kSmallMaxThreads
+               : (kSmallSmemInts / E - 3) * 32 < kSmallMinThreads ? kSmallMinThreads : (kSmallSmemInts / E - 3) * 32;
+}
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
@@ -214,21 +223,22 @@ __global__ void __launch_bounds__(kSlotThreads) route_slot_kernel(
 // MOE_BLOCK_M (thread t owns experts [t*per, t*per + per)), the row-block
 // tables, the padding rows, then the stable slots exactly as route_slot ranks
 // them (chunk base 0).  Also zeroes the error record and sets the bad-id bit.
-__global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
+__global__ void __launch_bounds__(kSmallMaxThreads) route_small_kernel(
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int n, int k, int E,
     int* __restrict__ count, int* __restrict__ off, int* __restrict__ poff, int* __restrict__ block_expert,
     int* __restrict__ block_rows, int* __restrict__ n_blocks, int* __restrict__ max_count, int* __restrict__ slot_of,
     int* __restrict__ row_token, int* __restrict__ row_topk, float* __restrict__ row_weight, int* __restrict__ err) {
     extern __shared__ int s_mem[];
+    const int nthreads = blockDim.x, nwarps = nthreads / 32;
     int* s_cnt = s_mem;                      // [E] counts, later the next free slot of each expert
-    int* s_wcnt = s_mem + E;                 // [kSmallWarps][E] same-expert counts per warp, this round
-    int* s_pad = s_mem + E * (1 + kSmallWarps);  // [2][E] padding rows [begin, end) of each expert
+    int* s_wcnt = s_mem + E;                 // [nwarps][E] same-expert counts per warp, this round
+    int* s_pad = s_mem + E * (1 + nwarps);   // [2][E] padding rows [begin, end) of each expert
     __shared__ int s_warp[32];
     __shared__ int s_max, s_bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int e = tid; e < E; e += kSmallThreads) {
+    for (int e = tid; e < E; e += nthreads) {
         s_cnt[e] = 0;
-        for (int w = 0; w < kSmallWarps; ++w) s_wcnt[w * E + e] = 0;
+        for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
     }
     if (tid == 0) {
         s_max = 0;
@@ -237,7 +247,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     __syncthreads();
     // 1. counts
     bool bad = false;
-    for (int i0 = 0; i0 < n; i0 += kSmallThreads) {
+    for (int i0 = 0; i0 < n; i0 += nthreads) {
         const int e = entry_expert(topk_idx, i0 + tid, n, E, &bad);
         const uint32_t same = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(same) - 1) atomicAdd(&s_cnt[e], __popc(same));
@@ -245,7 +255,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     if (bad) s_bad = 1;
     __syncthreads();
     // 2. scans over experts, per-thread runs of kSmallPerThread
-    const int per = (E + kSmallThreads - 1) / kSmallThreads;
+    const int per = (E + nthreads - 1) / nthreads;
     int c[kSmallPerThread];
     int sum_c = 0, sum_p = 0, mx = 0;
 #pragma unroll
@@ -291,15 +301,15 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
         err[1] = 0;
     }
     // padding rows: one warp per expert
-    for (int x = warp; x < E; x += kSmallWarps) {
+    for (int x = warp; x < E; x += nwarps) {
         for (int r = s_pad[x] + lane; r < s_pad[E + x]; r += 32) {
             row_token[r] = -1;
             row_topk[r] = -1;
             row_weight[r] = 0.0f;
         }
     }
-    // 3. stable slots, in rounds of kSmallThreads entries in flat order
-    for (int i0 = 0; i0 < n; i0 += kSmallThreads) {
+    // 3. stable slots, in rounds of blockDim entries in flat order
+    for (int i0 = 0; i0 < n; i0 += nthreads) {
         const int i = i0 + tid;
         bool unused = false;
         const int e = entry_expert(topk_idx, i, n, E, &unused);
@@ -342,8 +352,9 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
     int* poff = reinterpret_cast<int*>(ws + L.poff);
     int* chunk_base = reinterpret_cast<int*>(ws + L.chunk_base);
     if (L.chunks == 1) {  // one kernel for a decode-sized batch
-        const size_t smem = static_cast<size_t>(L.E) * (3 + kSmallWarps) * sizeof(int);
-        route_small_kernel<<<1, kSmallThreads, smem, s>>>(
+        const int threads = small_threads(L.E);
+        const size_t smem = static_cast<size_t>(L.E) * (3 + threads / 32) * sizeof(int);
+        route_small_kernel<<<1, threads, smem, s>>>(
             topk_idx, topk_w, static_cast<int>(n), L.k, L.E, count, off, poff,
             reinterpret_cast<int*>(ws + L.block_expert), reinterpret_cast<int*>(ws + L.block_rows),
             reinterpret_cast<int*>(ws + L.n_blocks), reinterpret_cast<int*>(ws + L.max_count),
