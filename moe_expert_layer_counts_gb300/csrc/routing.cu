@@ -30,9 +30,7 @@
 namespace moe {
 namespace {
 
-constexpr int kCountThreads = 256;
-constexpr int kSlotThreads = 256;
-constexpr int kSlotWarps = kSlotThreads / 32;
+constexpr int kCountThreads = 1024;
 constexpr int kScanThreads = 1024;
 // route_small runs as many warps (up to 32) as keep its shared memory, E x
 // (3 + warps) ints, within 47 KB (under the 48 KB default): 32 warps up to E = 343, 8 at
@@ -123,6 +121,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
     __shared__ int s_warp[32];
     __shared__ int s_max;
     __shared__ int s_pad[2][kScanThreads];  // padding rows [begin, end) of each expert
+    __shared__ int s_cnt[kScanThreads];     // count of each expert
     const int e = threadIdx.x;
     int c_e = 0;
     if (e == 0) s_max = 0;
@@ -150,39 +149,44 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
         }
         // s_max is final: the scans above passed block-wide barriers
         if (e == 0 && max_count) *max_count = s_max;
-        const int b0 = (inc_p - padded) / kBlockM;
-        for (int b = 0; b < padded / kBlockM; ++b) {
-            block_expert[b0 + b] = e;
-            if (block_rows) block_rows[b0 + b] = min(kBlockM, c_e - b * kBlockM);
-        }
         s_pad[0][e] = inc_p - padded + c_e;
         s_pad[1][e] = inc_p;
+        s_cnt[e] = c_e;
     }
-    if (!row_token) return;  // uniform: the counts-only path has no pool
     __syncthreads();
-    // padding rows (fewer than MOE_BLOCK_M per expert): one warp per expert
+    // the row-block tables and the padding rows' inverse maps: one warp per expert
     const int lane = threadIdx.x & 31;
     for (int x = threadIdx.x >> 5; x < E; x += kScanThreads / 32) {
-        for (int r = s_pad[0][x] + lane; r < s_pad[1][x]; r += 32) {
-            row_token[r] = -1;
-            row_topk[r] = -1;
-            row_weight[r] = 0.0f;
+        const int c_x = s_cnt[x], end = s_pad[1][x];
+        const int nb = (c_x + kBlockM - 1) / kBlockM;
+        const int b0 = end / kBlockM - nb;
+        for (int b = lane; b < nb; b += 32) {
+            block_expert[b0 + b] = x;
+            if (block_rows) block_rows[b0 + b] = min(kBlockM, c_x - b * kBlockM);
+        }
+        if (row_token) {
+            for (int r = s_pad[0][x] + lane; r < end; r += 32) {
+                row_token[r] = -1;
+                row_topk[r] = -1;
+                row_weight[r] = 0.0f;
+            }
         }
     }
 }
 
-__global__ void __launch_bounds__(kSlotThreads) route_slot_kernel(
+__global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
     const int* __restrict__ poff, const int* __restrict__ chunk_base,
     int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
     float* __restrict__ row_weight) {
     extern __shared__ int s_mem[];
+    const int nwarps = blockDim.x / 32;
     int* s_next = s_mem;        // [E] next free slot of each expert for this chunk
-    int* s_wcnt = s_mem + E;    // [kSlotWarps][E] same-expert counts per warp, this round
+    int* s_wcnt = s_mem + E;    // [nwarps][E] same-expert counts per warp, this round
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         s_next[e] = poff[e] + chunk_base[static_cast<size_t>(blockIdx.x) * E + e];
-        for (int w = 0; w < kSlotWarps; ++w) s_wcnt[w * E + e] = 0;
+        for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
     }
     __syncthreads();
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
@@ -378,8 +382,9 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
                                                  reinterpret_cast<float*>(ws + L.row_weight));
     if ((st = cudaGetLastError()) != cudaSuccess) return st;
     if (L.chunks > 0) {
-        const size_t smem = static_cast<size_t>(L.E) * (1 + kSlotWarps) * sizeof(int);
-        route_slot_kernel<<<L.chunks, kSlotThreads, smem, s>>>(
+        const int threads = small_threads(L.E);  // its shared memory, E x (1 + warps) ints, fits as well
+        const size_t smem = static_cast<size_t>(L.E) * (1 + threads / 32) * sizeof(int);
+        route_slot_kernel<<<L.chunks, threads, smem, s>>>(
             topk_idx, topk_w, n, L.k, L.E, poff, chunk_base, reinterpret_cast<int*>(ws + L.slot_of),
             reinterpret_cast<int*>(ws + L.row_token), reinterpret_cast<int*>(ws + L.row_topk),
             reinterpret_cast<float*>(ws + L.row_weight));
