@@ -67,15 +67,17 @@ def test_plan_edge_cases(moe, oracle):
 
 
 @pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096])
-def test_plan_one_kernel_and_chunked_paths(moe, oracle, n):
+@pytest.mark.parametrize("E", [8, 300, 512, 1024])
+def test_plan_one_kernel_and_chunked_paths(moe, oracle, n, E):
     """Up to 2048 entries the plan is one single-CTA kernel, above it the
     chunked count / scan / slot kernels: both sides of the switch, with
-    skipped and bad ids and 1024 experts."""
-    rng = np.random.default_rng(n)
-    idx = rng.integers(-1, 1024, size=(n, 1))
+    skipped and bad ids; the expert counts give the routing kernels 1024,
+    1024, 640 and 256 threads."""
+    rng = np.random.default_rng(n + E)
+    idx = rng.integers(-1, E, size=(n, 1))
     if n > 3:
-        idx[n // 2, 0] = 1024
-    compare_plan(moe, oracle, idx, rng.random((n, 1)), 1024)
+        idx[n // 2, 0] = E
+    compare_plan(moe, oracle, idx, rng.random((n, 1)), E)
 
 
 def test_empty_batch(moe):
