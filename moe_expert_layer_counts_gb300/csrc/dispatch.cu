@@ -8,7 +8,8 @@
 // the quantisation is fused into the gather: each token row is read once,
 // quantised once (E4M3 codes, one UE8M0 byte per 32 elements), and written to
 // each of its k pool rows.  One warp handles a 1024-element segment of one
-// token; a lane owns 8 consecutive elements, four lanes one 32-block.
+// token; a lane owns 16 consecutive elements (two 16-byte loads, one 16-byte
+// store per pool row), two lanes one 32-block.
 // Scales are written directly in the tensor-core layout the GEMM consumes:
 // chunk (row/128, col/128) of 512 bytes, byte 16*(row%32) + 4*((row%128)/32)
 // + (col/32)%4.
@@ -36,34 +37,41 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
     const int my_slot = lane < k ? __ldg(slot_of + static_cast<size_t>(t) * k + lane) : -1;
     const int s_begin = seg * kSeg, s_end = min(s_begin + kSeg, H);
     const int sf_cols = H / 128;
-    for (int s0 = s_begin; s0 < s_end; s0 += 256) {
-        const int col = s0 + lane * 8;
-        const bool active = col < s_end;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (active) raw = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + col));
-        float f[8] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y),
-                      bf16_lo(raw.z), bf16_hi(raw.z), bf16_lo(raw.w), bf16_hi(raw.w)};
+    for (int s0 = s_begin; s0 < s_end; s0 += 512) {
+        const int col = s0 + lane * 16;
+        const bool active = col < s_end;  // H is a multiple of 128: a lane's 16 columns are all in or all out
+        uint4 raw0 = make_uint4(0, 0, 0, 0), raw1 = make_uint4(0, 0, 0, 0);
+        if (active) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + col);
+            raw0 = __ldg(src);
+            raw1 = __ldg(src + 1);
+        }
+        float f[16] = {bf16_lo(raw0.x), bf16_hi(raw0.x), bf16_lo(raw0.y), bf16_hi(raw0.y),
+                       bf16_lo(raw0.z), bf16_hi(raw0.z), bf16_lo(raw0.w), bf16_hi(raw0.w),
+                       bf16_lo(raw1.x), bf16_hi(raw1.x), bf16_lo(raw1.y), bf16_hi(raw1.y),
+                       bf16_lo(raw1.z), bf16_hi(raw1.z), bf16_lo(raw1.w), bf16_hi(raw1.w)};
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const uint32_t sbyte = ue8m0_scale_e4m3_rule(amax, scale_rule);
         const float inv = inv_scale_from_byte(sbyte);
-        uint2 codes;
+        uint4 codes;
         codes.x = e4m3x2(f[0] * inv, f[1] * inv) | (e4m3x2(f[2] * inv, f[3] * inv) << 16);
         codes.y = e4m3x2(f[4] * inv, f[5] * inv) | (e4m3x2(f[6] * inv, f[7] * inv) << 16);
-        // scale word of the 128-column group owned by lanes 0..15 / 16..31
-        const int g = lane & 16;
-        const uint32_t sw = __shfl_sync(0xffffffffu, sbyte, g) | (__shfl_sync(0xffffffffu, sbyte, g + 4) << 8) |
-                            (__shfl_sync(0xffffffffu, sbyte, g + 8) << 16) |
-                            (__shfl_sync(0xffffffffu, sbyte, g + 12) << 24);
+        codes.z = e4m3x2(f[8] * inv, f[9] * inv) | (e4m3x2(f[10] * inv, f[11] * inv) << 16);
+        codes.w = e4m3x2(f[12] * inv, f[13] * inv) | (e4m3x2(f[14] * inv, f[15] * inv) << 16);
+        // scale word of the 128-column group owned by lanes 8g..8g+7 (two lanes per 32-block)
+        const int g = lane & 24;
+        const uint32_t sw = __shfl_sync(0xffffffffu, sbyte, g) | (__shfl_sync(0xffffffffu, sbyte, g + 2) << 8) |
+                            (__shfl_sync(0xffffffffu, sbyte, g + 4) << 16) |
+                            (__shfl_sync(0xffffffffu, sbyte, g + 6) << 24);
         for (int j = 0; j < k; ++j) {
             const int r = __shfl_sync(0xffffffffu, my_slot, j);
             if (r < 0) continue;
             if (active) {
-                *reinterpret_cast<uint2*>(pool_q + static_cast<size_t>(r) * H + col) = codes;
-                if ((lane & 15) == 0) {
+                *reinterpret_cast<uint4*>(pool_q + static_cast<size_t>(r) * H + col) = codes;
+                if ((lane & 7) == 0) {
                     const size_t chunk = static_cast<size_t>(r / kBlockM) * sf_cols + col / 128;
                     const int m = r % kBlockM;
                     *reinterpret_cast<uint32_t*>(pool_sf + chunk * kSfChunkBytes + 16 * (m % 32) + 4 * (m / 32)) =
