@@ -160,8 +160,8 @@ __device__ __noinline__ float silu_exact(float g) {
 // __expf and an approximate divide (error well below kDecisionUlps for
 // |gate| <= 16).  Wherever that could change an integer decision under the
 // exact formula, the exact value is used instead: an element with
-// |gate| > 16 or within kDecisionUlps of an E4M3 code midpoint is recomputed
-// alone; if the block maximum lies that close to the UE8M0 scale boundary,
+// |gate| > 16, or with a rounding boundary of the E4M3 grid within
+// kDecisionUlps of it, is recomputed alone; if the block maximum lies that close to the UE8M0 scale boundary,
 // the whole block is recomputed.  So every code and scale byte is the one the
 // exact definition gives.  The fast path is branch-free (it only collects
 // bit masks), so the 32 values are computed with full instruction-level
@@ -225,15 +225,32 @@ __device__ __forceinline__ uint32_t requant_block(const uint32_t* gu, float wgt,
     }
     const uint32_t sbyte = ue8m0_scale_e4m3_rule(amax, scale_rule);
     const float inv = inv_scale_from_byte(sbyte);
-    // 3. the codes: values near a rounding midpoint go exact
+    // 3. the codes.  The E4M3 codes of q*(1-eps) and q*(1+eps), eps = kDecisionUlps
+    // * 2^-23 (at least kDecisionUlps ulps of q), are equal unless a rounding
+    // boundary of the E4M3 grid (normal or subnormal) lies within the band;
+    // then the fast value could round differently from the exact one and goes
+    // exact.  Otherwise either code is the exact value's code.
+    constexpr float kLo = 1.0f - static_cast<float>(kDecisionUlps) * 0x1p-23f;
+    constexpr float kHi = 1.0f + static_cast<float>(kDecisionUlps) * 0x1p-23f;
     uint32_t near = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) near |= static_cast<uint32_t>(near_e4m3_midpoint(h[i] * inv, kDecisionUlps)) << i;
-    if (near) fixup(gu, wgt, clamp, h, near);
     uint32_t q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        q[i] = e4m3x2(h[4 * i] * inv, h[4 * i + 1] * inv) | (e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv) << 16);
+    for (int i = 0; i < 16; ++i) {
+        const float q0 = h[2 * i] * inv, q1 = h[2 * i + 1] * inv;
+        const uint32_t a = e4m3x2(q0 * kLo, q1 * kLo), c = e4m3x2(q0 * kHi, q1 * kHi);
+        const uint32_t d = a ^ c;
+        near |= (static_cast<uint32_t>((d & 0xFFu) != 0u) | (static_cast<uint32_t>((d & 0xFF00u) != 0u) << 1)) << (2 * i);
+        if (i & 1)
+            q[i >> 1] |= a << 16;
+        else
+            q[i >> 1] = a;
+    }
+    if (near) {
+        fixup(gu, wgt, clamp, h, near);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            q[i] = e4m3x2(h[4 * i] * inv, h[4 * i + 1] * inv) | (e4m3x2(h[4 * i + 2] * inv, h[4 * i + 3] * inv) << 16);
+    }
     uint4* d = reinterpret_cast<uint4*>(dst);
     d[0] = make_uint4(q[0], q[1], q[2], q[3]);
     d[1] = make_uint4(q[4], q[5], q[6], q[7]);

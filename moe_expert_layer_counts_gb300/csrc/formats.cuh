@@ -60,30 +60,6 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// True when |q| (a value already divided by its block scale) lies within
-// `ulps` fp32 ulps of a rounding midpoint of the E4M3 grid, i.e. when a
-// slightly different q could round to another code.  Normal E4M3 values keep
-// 3 mantissa bits, so the dropped part is the low 20 bits of the fp32
-// mantissa; below 2^-6 the grid is uniform with step 2^-9 and more bits drop.
-__device__ __forceinline__ bool near_e4m3_midpoint(float q, uint32_t ulps) {
-    const uint32_t b = __float_as_uint(q) & 0x7FFFFFFFu;
-    const int ex = static_cast<int>(b >> 23) - 127;
-    if (ex >= -6) {
-        const uint32_t low = b & 0xFFFFFu;
-        const uint32_t d = low > 0x80000u ? low - 0x80000u : 0x80000u - low;
-        return d <= ulps;
-    }
-    const int drop = 20 + (-6 - ex);  // bits below the 2^-9 grid step
-    if (drop >= 24) {  // q < 2^-9: the only midpoint nearby is 2^-10 (bits 0x3A800000)
-        const uint32_t d = b > 0x3A800000u ? b - 0x3A800000u : 0x3A800000u - b;
-        return d <= ulps;
-    }
-    const uint32_t mant = (b & 0x7FFFFFu) | 0x800000u;
-    const uint32_t low = mant & ((1u << drop) - 1u), half = 1u << (drop - 1);
-    const uint32_t d = low > half ? low - half : half - low;
-    return d <= ulps;
-}
-
 // True when amax lies within `ulps` of the E4M3 scale boundary (mantissa
 // 1.75, where ue8m0_scale_e4m3 changes exponent).
 __device__ __forceinline__ bool near_e4m3_scale_boundary(float amax, uint32_t ulps) {
