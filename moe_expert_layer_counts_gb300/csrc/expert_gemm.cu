@@ -161,9 +161,9 @@ __device__ __noinline__ float silu_exact(float g) {
 // |gate| <= 16).  Wherever that could change an integer decision under the
 // exact formula, the exact value is used instead: an element with
 // |gate| > 16, or with a rounding boundary of the E4M3 grid within
-// kDecisionUlps of it, is recomputed alone; if the block maximum lies that close to the UE8M0 scale boundary,
-// the whole block is recomputed.  So every code and scale byte is the one the
-// exact definition gives.  The fast path is branch-free (it only collects
+// kDecisionUlps of it, is recomputed alone; if the block maximum lies that
+// close to the UE8M0 scale boundary, the whole block is recomputed.  So every
+// code and scale byte is the one the exact definition gives.  The fast path is branch-free (it only collects
 // bit masks), so the 32 values are computed with full instruction-level
 // parallelism.  Writes 32 E4M3 codes to dst (16-byte aligned) and returns the
 // scale byte.
