@@ -1,8 +1,8 @@
 """Benchmark of the fused MoE layer forward on GB300.
 
 One step = the whole hot path on one batch: moe_plan (route_count,
-route_scan, route_slot) + moe_forward (dispatch_quant, expert L1, expert L2,
-combine), on the full skewed workload T=8192, H=7168, I=2048, E=256, k=8 by
+route_scan, route_slot; route_small alone for at most 2048 top-k entries) +
+moe_forward (dispatch_quant, expert L1, expert L2, combine), on the full skewed workload T=8192, H=7168, I=2048, E=256, k=8 by
 default.  Inputs are synthetic and seeded, resident in HBM before timing;
 L2 is flushed (a 512 MB buffer is written) before every timed step, outside
 the timed events.  FLOPs = 6 * N * H * I with N the number of valid top-k
@@ -35,7 +35,14 @@ from moe_expert_layer_counts_gb300 import inputs  # noqa: E402
 
 METRIC = "MoE fwd TFLOP/s & tokens/s (T=8192,H=7168,I=2048,E=256,k=8); % FP8 peak"
 STAGES = ("route", "dispatch", "expert_l1", "expert_l2", "combine")
-KERNELS_PER_STEP = 7  # route_count, route_scan, route_slot, dispatch_quant, L1, L2, combine
+ROUTE_CHUNK = 2048  # top-k entries the one-kernel plan handles
+
+
+def kernels_per_step(w) -> int:
+    """Kernels of the library one step launches: the plan (route_count,
+    route_scan, route_slot, or route_small for at most ROUTE_CHUNK top-k
+    entries), dispatch_quant, the two expert GEMMs and combine."""
+    return (1 if w.T * w.k <= ROUTE_CHUNK else 3) + 4
 FLUSH_BYTES = 512 << 20
 
 
@@ -426,7 +433,7 @@ def main():
                              note="one step at a time: copy in, plan, forward, copy out, wait"),
                  graph=dict(value=graph_val, unit="TFLOP/s", ms_per_step=1e3 * graph_t / args.e2e_steps,
                             note="one step at a time, captured once in a CUDA graph and replayed")),
-        gpu_launches=KERNELS_PER_STEP * args.steps,
+        gpu_launches=kernels_per_step(w) * args.steps,
         clocks=clk.summary(),
         cpu_baseline=cpu,
     )
