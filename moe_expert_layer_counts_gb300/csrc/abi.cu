@@ -223,7 +223,7 @@ int moe_dispatch(const moe_plan_t* plan, const void* x, const moe_options_t* opt
     if (!ps || (ps->T > 0 && !x) || (reinterpret_cast<uintptr_t>(x) & 15u)) return MOE_ERR_INVALID_ARG;
     if (!read_options(opts, &o)) return MOE_ERR_INVALID_ARG;
     Layout L;
-    make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
+    if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
     int rc = device_info(nullptr);
     if (rc) return rc;
     return cuda_status(launch_dispatch(L, ps->ws, x, o.scale_rule, static_cast<cudaStream_t>(stream)));
@@ -241,7 +241,7 @@ static int expert_layer(int layer, const moe_plan_t* plan, const moe_weights_t* 
     int sms = 0;
     if ((rc = device_info(&sms))) return rc;
     Layout L;
-    make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
+    if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
     GemmLaunch g{W->q, W->sf_mma, W->E, W->N, W->K, o.activation_clamp, o.scale_rule, o.fast_math};
     return cuda_status(launch_expert_gemm(layer, L, ps->ws, g, sms, static_cast<cudaStream_t>(stream)));
 }
@@ -260,7 +260,7 @@ int moe_combine(const moe_plan_t* plan, void* y, void* stream) {
     int rc = device_info(nullptr);
     if (rc) return rc;
     Layout L;
-    make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
+    if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
     return cuda_status(launch_combine(L, ps->ws, y, static_cast<cudaStream_t>(stream)));
 }
 
@@ -279,7 +279,7 @@ int moe_plan_check(const moe_plan_t* plan, void* stream) {
     const PlanState* ps = plan_state(plan);
     if (!ps) return MOE_ERR_INVALID_ARG;
     Layout L;
-    make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
+    if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
     int err = 0;
     if (cudaMemcpy(&err, ps->ws + L.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
@@ -292,7 +292,7 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
     const PlanState* ps = plan_state(plan);
     if (!ps || !offset || !bytes) return MOE_ERR_INVALID_ARG;
     Layout L;
-    make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L);
+    if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
     const size_t cap = static_cast<size_t>(L.p_cap);
     const size_t n = static_cast<size_t>(ps->T) * ps->k;
     switch (what) {

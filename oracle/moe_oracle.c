@@ -468,7 +468,7 @@ void or_l2_row(const uint8_t* hq, const uint8_t* hsf, const uint8_t* w2q, const 
 int or_bruteforce_token(const uint16_t* x_row, const int64_t* idx_row, const float* w_row, int k, int E,
                         int H, int I, const uint8_t* w1q, const uint8_t* w1sf,
                         const uint8_t* w2q, const uint8_t* w2sf, float clamp, int rule, uint16_t* y_row) {
-    float* xf = (float*)malloc(sizeof(float) * H);
+    float* xf = (float*)calloc(H > 0 ? H : 1, sizeof(float));
     uint8_t* xq = (uint8_t*)malloc(H);
     uint8_t* xsf = (uint8_t*)malloc(H / OR_SF_VEC + 1);
     float* h = (float*)malloc(sizeof(float) * I);
