@@ -1,7 +1,6 @@
 """Failure detection without a GPU fault: the library's bounded mbarrier wait
 gives up at its deadline and reports MOE_ERR_TIMEOUT, and the context stays
 usable afterwards."""
-import numpy as np
 import pytest
 
 import gpu_helpers as gh

@@ -4,7 +4,6 @@ import math
 import os
 
 import numpy as np
-import pytest
 import torch
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
