@@ -82,8 +82,6 @@ def lib():
                                      ctypes.c_float, i32, i32]
             L.or_combine.restype = None
             L.or_combine.argtypes = [P, P, i32, i32, i32, P]
-            L.or_l2_row.restype = None
-            L.or_l2_row.argtypes = [P, P, P, P, i32, i32, i32, P]
             L.or_bruteforce_token.restype = i32
             L.or_bruteforce_token.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, P, ctypes.c_float, i32, P]
             L.or_num_threads.restype = i32
@@ -207,7 +205,8 @@ def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
     [E,2I,H/32]; w2q uint8 [E,H,I/2]; w2sf uint8 [E,H,I/32].
     tokens: optional int array of tokens to compute (y rows in that order).
     want_pool: also return per-pool-row hq [p_cap,I], hsf [p_cap,I/32], o [p_cap,H] and the
-    pre-requantisation h [p_cap,I] (float32).
+    pre-requantisation h [p_cap,I] (float32); with a token subset only the pool rows of those
+    tokens are filled (the others stay zero).
     activation_clamp: > 0 limits the bf16 gate and up values to [-c, c] before SwiGLU.
     scale_rule: SCALE_RULE_CEIL or SCALE_RULE_OCP_FLOOR for the activation (x and h) scales.
     Returns dict(y=uint16 bf16 bits, status, and pool arrays if asked)."""
@@ -229,7 +228,7 @@ def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
         toks_p, ntok = _p(toks), toks.size
     y = np.zeros((ntok, H), np.uint16)
     hq = hsf = o = hf = None
-    if want_pool and tokens is None:
+    if want_pool:
         hq = np.zeros((p_cap, I), np.uint8)
         hsf = np.zeros((p_cap, I // SF_VEC), np.uint8)
         o = np.zeros((p_cap, H), np.uint16)
@@ -252,18 +251,6 @@ def combine(o_pool: np.ndarray, slot_of: np.ndarray, T: int, k: int):
     y = np.zeros((T, H), np.uint16)
     lib().or_combine(_p(o), _p(s), T, k, H, _p(y))
     return y
-
-
-def l2_row(hq_row, hsf_row, w2q, w2sf, e: int):
-    hq = _c(hq_row, np.uint8)
-    hsf = _c(hsf_row, np.uint8)
-    w2q = _c(w2q, np.uint8)
-    w2sf = _c(w2sf, np.uint8)
-    H = w2q.shape[1]
-    I = w2q.shape[2] * 2
-    o = np.zeros(H, np.uint16)
-    lib().or_l2_row(_p(hq), _p(hsf), _p(w2q), _p(w2sf), e, H, I, _p(o))
-    return o
 
 
 def bruteforce_token(x_row_bits, idx_row, w_row, E, w1q, w1sf, w2q, w2sf, activation_clamp: float = 0.0,

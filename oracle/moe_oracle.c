@@ -320,7 +320,8 @@ void or_quant_x(const uint16_t* x, int T, int H, int rule, uint8_t* q, uint8_t* 
 
 /* Forward pass.  tokens == NULL computes every token; otherwise only the
  * ntok listed tokens, with y rows written in list order ([ntok, H]).
- * Optional per-pool-row outputs (only when tokens == NULL; may be NULL):
+ * Optional per-pool-row outputs (may be NULL), written for the pool rows of
+ * the computed tokens only (other rows are left as they are):
  *   hq_pool [p_cap, I], hsf_pool [p_cap, I/32], o_pool [p_cap, H] (bf16 bits),
  *   h_pool [p_cap, I] (fp32 SwiGLU*w before requantisation).
  * Work is done expert by expert over the expert-major pool, each expert's
@@ -394,12 +395,10 @@ int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
                 ffn_row(xq + (size_t)t * H, xsf + (size_t)t * (H / OR_SF_VEC), w1d, w2d, H, I,
                         row_weight[r], clamp, rule, xd, hd, h, hq, hsf, o);
                 memcpy(o_ent + ((size_t)want[t] * k + j) * H, o, sizeof(uint16_t) * H);
-                if (!tokens) {
-                    if (hq_pool) memcpy(hq_pool + (size_t)r * I, hq, (size_t)I);
-                    if (hsf_pool) memcpy(hsf_pool + (size_t)r * (I / OR_SF_VEC), hsf, (size_t)I / OR_SF_VEC);
-                    if (o_pool) memcpy(o_pool + (size_t)r * H, o, sizeof(uint16_t) * H);
-                    if (h_pool) memcpy(h_pool + (size_t)r * I, h, sizeof(float) * I);
-                }
+                if (hq_pool) memcpy(hq_pool + (size_t)r * I, hq, (size_t)I);
+                if (hsf_pool) memcpy(hsf_pool + (size_t)r * (I / OR_SF_VEC), hsf, (size_t)I / OR_SF_VEC);
+                if (o_pool) memcpy(o_pool + (size_t)r * H, o, sizeof(uint16_t) * H);
+                if (h_pool) memcpy(h_pool + (size_t)r * I, h, sizeof(float) * I);
             }
             free(xd); free(hd); free(h); free(hq); free(hsf); free(o);
         }
@@ -439,25 +438,6 @@ void or_combine(const uint16_t* o_pool, const int32_t* slot_of, int T, int k, in
             }
             y[(size_t)t * H + c] = or_bf16_encode(acc);
         }
-    }
-}
-
-/* L2 alone for given requantised activations (one row): used to check the
- * GPU L2 on identical inputs. hq/hsf [I], W2 of expert e -> o [H] bf16. */
-void or_l2_row(const uint8_t* hq, const uint8_t* hsf, const uint8_t* w2q, const uint8_t* w2sf,
-               int e, int H, int I, uint16_t* o) {
-    const uint8_t* qe = w2q + (size_t)e * H * (I / 2);
-    const uint8_t* se = w2sf + (size_t)e * H * (I / OR_SF_VEC);
-    for (int c = 0; c < H; ++c) {
-        double acc = 0.0;
-        for (int i = 0; i < I; ++i) {
-            uint8_t byte = qe[(size_t)c * (I / 2) + i / 2];
-            int nib = (i % 2 == 0) ? (byte & 15) : (byte >> 4);
-            double w = or_e2m1_decode(nib) * or_ue8m0_value(se[(size_t)c * (I / OR_SF_VEC) + i / OR_SF_VEC]);
-            double a = or_e4m3_decode(hq[i]) * or_ue8m0_value(hsf[i / OR_SF_VEC]);
-            acc += a * w;
-        }
-        o[c] = or_bf16_encode((float)acc);
     }
 }
 

@@ -36,10 +36,15 @@ def test_bruteforce_matches_pool_oracle(oracle, T, H, I, E, k):
         yb, st = oracle.bruteforce_token(x[t], idx[t], tw[t], E, *args)
         assert st == 0
         np.testing.assert_array_equal(yb, res["y"][t])
-    # a token subset gives the same rows
+    # a token subset gives the same rows, and the same pool rows for its entries
     sub = np.array([5, 0, T - 1], np.int32)
-    rs = oracle.forward(x, idx, tw, E, *args, tokens=sub)
+    rs = oracle.forward(x, idx, tw, E, *args, tokens=sub, want_pool=True)
     np.testing.assert_array_equal(rs["y"], res["y"][sub])
+    full = oracle.forward(x, idx, tw, E, *args, want_pool=True)
+    rows = oracle.plan(idx, tw, E)["slot_of"].reshape(T, k)[sub].ravel()
+    rows = rows[rows >= 0]
+    for key in ("hq", "hsf", "o", "h"):
+        np.testing.assert_array_equal(rs[key][rows], full[key][rows])
 
 
 def _ue8m0(a, m):
@@ -83,16 +88,11 @@ def _mx8_torch(v64: torch.Tensor):
     return out.reshape(v64.shape)
 
 
-def test_dense_special_case_against_torch(oracle):
-    """E=1, k=1, w=1: the layer is a dense quantised FFN; recompute it with
-    torch matmuls and torch's E4M3/bf16 casts."""
-    T, H, I = 16, 128, 64
-    w, d = _small(T, H, I, 1, 1, seed=3)
-    idx = np.zeros((T, 1), np.int64)
-    tw = np.ones((T, 1), np.float32)
-    args = [a.numpy() for a in (d["w1q"], d["w1sf"], d["w2q"], d["w2sf"])]
-    y = oracle.forward(_bits(d["x"]), idx, tw, 1, *args)["y"]
-
+def _dense_torch(d, I, weight, w_in_epilogue=True):
+    """E=1, k=1 layer rebuilt from torch float64 matmuls and torch's E4M3 /
+    bf16 casts.  The top-k weight multiplies the SwiGLU output before the
+    requantisation (page "Dispatch/Combine in the DeepGEMM Mega MoE kernel",
+    section 4.2), or -- the reading this test must reject -- the L2 output."""
     tab = _golden_e2m1()
     W1 = _deq_w(d["w1q"][0], d["w1sf"][0], tab)  # [2I, H]
     W2 = _deq_w(d["w2q"][0], d["w2sf"][0], tab)  # [H, I]
@@ -100,14 +100,77 @@ def test_dense_special_case_against_torch(oracle):
     acc = (xq @ W1.T).to(torch.float32).to(torch.bfloat16).to(torch.float64)
     g, u = acc[:, :I], acc[:, I:]
     silu = (g / (1.0 + torch.exp(-g))).to(torch.float32)
-    h = (silu * u.to(torch.float32)) * 1.0
+    wt = torch.tensor(weight, dtype=torch.float32)
+    h = silu * u.to(torch.float32)
+    if w_in_epilogue:
+        h = h * wt
     hq = _mx8_torch(h.to(torch.float64))
     o = (hq @ W2.T).to(torch.float32).to(torch.bfloat16)
+    if not w_in_epilogue:
+        o = (o.to(torch.float32) * wt).to(torch.bfloat16)
+    return o
+
+
+@pytest.mark.parametrize("weight", [1.0, 0.73])
+def test_dense_special_case_against_torch(oracle, weight):
+    """E=1, k=1: the layer is a dense quantised FFN scaled by the one top-k
+    weight; recompute it with torch matmuls and torch's E4M3/bf16 casts.  With
+    a weight that is not a power of two (0.73, the pages' example weight) the
+    requantisation of h is not scale-invariant, so the position of the weight
+    matters: the oracle must agree with the weight applied to h before the
+    requant, and must not agree with it applied to the L2 output."""
+    T, H, I = 16, 128, 64
+    w, d = _small(T, H, I, 1, 1, seed=3)
+    idx = np.zeros((T, 1), np.int64)
+    tw = np.full((T, 1), weight, np.float32)
+    args = [a.numpy() for a in (d["w1q"], d["w1sf"], d["w2q"], d["w2sf"])]
+    y = oracle.forward(_bits(d["x"]), idx, tw, 1, *args)["y"]
+
+    o = _dense_torch(d, I, weight)
     ref = o.view(torch.int16).numpy().astype(np.uint16)
     mism = np.mean(ref != y)
     assert mism <= 1e-3, mism
     yf = torch.from_numpy(y.astype(np.int16)).view(torch.bfloat16).double()
     assert torch.linalg.norm(yf - o.double()) <= 1e-3 * torch.linalg.norm(o.double())
+    if weight != 1.0:
+        wrong = _dense_torch(d, I, weight, w_in_epilogue=False).view(torch.int16).numpy().astype(np.uint16)
+        assert np.mean(wrong != y) > 0.05, np.mean(wrong != y)
+
+
+def test_combine_against_numpy_sum(oracle):
+    """or_combine against an independent restatement: numpy float32 adds of
+    the bf16 rows in ascending j (skipping -1 slots, from +0), then one round
+    to bf16 by torch's cast (round to nearest even); tokens without a valid
+    slot give +0 (page "DeepEP -> Mega MoE", combine_utils.cuh snippet; page
+    "Dispatch/Combine in the DeepGEMM Mega MoE kernel", section 5.1)."""
+    rng = np.random.default_rng(21)
+    T, k, H, P = 40, 6, 96, 300
+    rows = torch.from_numpy(rng.standard_normal((P, H)) * np.exp2(rng.integers(-14, 14, (P, 1))))
+    o_pool = rows.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    slot_of = rng.integers(0, P, (T, k)).astype(np.int32)
+    slot_of[rng.random((T, k)) < 0.3] = -1
+    slot_of[7] = -1                      # a token without a valid entry
+    y = oracle.combine(o_pool, slot_of.ravel(), T, k)
+    vals = torch.from_numpy(o_pool.view(np.int16)).view(torch.bfloat16).float().numpy()
+    ref = np.zeros((T, H), np.float32)
+    for t in range(T):
+        acc = np.zeros(H, np.float32)
+        for j in range(k):
+            if slot_of[t, j] >= 0:
+                acc = (acc + vals[slot_of[t, j]]).astype(np.float32)
+        ref[t] = acc
+    ref_bits = torch.from_numpy(ref).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(y, ref_bits)
+    assert np.all(y[7] == 0)
+    # the order of the adds is visible: summing the same rows in descending j differs somewhere
+    rev = np.zeros((T, H), np.float32)
+    for t in range(T):
+        acc = np.zeros(H, np.float32)
+        for j in reversed(range(k)):
+            if slot_of[t, j] >= 0:
+                acc = (acc + vals[slot_of[t, j]]).astype(np.float32)
+        rev[t] = acc
+    assert np.any(rev != ref)
 
 
 def test_identical_experts_identity(oracle):
