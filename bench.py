@@ -2,11 +2,15 @@
 
 One step = the whole hot path on one batch: moe_plan (route_count,
 route_scan, route_slot; route_small alone for at most 2048 top-k entries) +
-moe_forward (dispatch_quant, expert L1, expert L2, combine), on the full skewed workload T=8192, H=7168, I=2048, E=256, k=8 by
-default.  Inputs are synthetic and seeded, resident in HBM before timing;
-L2 is flushed (a 512 MB buffer is written) before every timed step, outside
-the timed events.  FLOPs = 6 * N * H * I with N the number of valid top-k
-entries.
+moe_forward (dispatch_quant, expert L1, expert L2, combine), on the full
+skewed workload T=8192, H=7168, I=2048, E=256, k=8 by default.  Inputs are
+synthetic and seeded, resident in HBM before timing; L2 is flushed (a 512 MB
+buffer is written) before every timed step, outside the timed events.
+FLOPs = 6 * N * H * I with N the number of valid top-k entries.
+
+The default run also times the decode-shaped workload (T=128, same layer
+sizes), whose bound is the weight stream from HBM, and reports it in a
+`decode` object of the same JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload full]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
@@ -36,6 +40,9 @@ from moe_expert_layer_counts_gb300 import inputs  # noqa: E402
 METRIC = "MoE fwd TFLOP/s & tokens/s (T=8192,H=7168,I=2048,E=256,k=8); % FP8 peak"
 STAGES = ("route", "dispatch", "expert_l1", "expert_l2", "combine")
 ROUTE_CHUNK = 2048  # top-k entries the one-kernel plan handles
+FLUSH_BYTES = 512 << 20
+# FLOPs of one oracle sample (about 7 s on 16 host cores at the full layer size)
+ORACLE_SAMPLE_FLOP = 4.0e11
 
 
 def kernels_per_step(w) -> int:
@@ -43,12 +50,13 @@ def kernels_per_step(w) -> int:
     route_scan, route_slot, or route_small for at most ROUTE_CHUNK top-k
     entries), dispatch_quant, the two expert GEMMs and combine."""
     return (1 if w.T * w.k <= ROUTE_CHUNK else 3) + 4
-FLUSH_BYTES = 512 << 20
 
 
 def peaks():
-    """Roofline denominators: measured copy bandwidth and bf16 GEMM rate of
-    this GPU pool; FP8 (the MXF8F6F4 rate) taken as 2x the bf16 rate."""
+    """Roofline denominators measured on this GPU pool: copy bandwidth and the
+    bf16 GEMM rate as a burst (the GEMMs here are timed inside a short run of
+    steps at the maximum SM clock); FP8 (the MXF8F6F4 rate) is 2x bf16, the
+    nominal ratio of the two dense tensor rates."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         m = json.load(open(path))
@@ -136,150 +144,155 @@ def kernel_source_hash() -> str:
     return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
 
 
-def measured_traffic():
+def measured_traffic(workload: str):
     """Per-launch DRAM bytes of the L1 kernel on this workload from the
     committed ncu summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "expert_l1_traffic.json")
     if not os.path.exists(path):
         return None
     m = json.load(open(path))
-    return m.get("bytes_per_launch") if m.get("kernel_sha") == kernel_source_hash() else None
+    if m.get("kernel_sha") != kernel_source_hash():
+        return None
+    return m.get("bytes_per_launch", {}).get(workload)
 
 
-def cpu_baseline(w, d, target_s: float):
-    """The oracle, as it stands, on the host cores: an evenly spaced token
-    sample sized (from a 64-token calibration run) to about target_s seconds."""
+# ------------------------------------------------------------------ oracle legs
+def oracle_sample(w):
+    """The token sample both oracle timings (cpu_baseline and the reference
+    arm) use: evenly spaced tokens, as many as make about ORACLE_SAMPLE_FLOP
+    of layer work at k entries per token (all tokens of the small
+    workloads)."""
     import numpy as np
-    import oracle
-    oracle.build()
+    n = min(w.T, max(32, int(ORACLE_SAMPLE_FLOP / (6.0 * w.H * w.I * w.k))))
+    step = max(1, w.T // n)
+    return np.arange(0, w.T, step, dtype=np.int32)[:n], step
+
+
+def _oracle_args(d):
+    import numpy as np
     x = d["x"].cpu().view(torch.int16).numpy().view(np.uint16)
     idx = d["topk_idx"].cpu().numpy()
     tw = d["topk_w"].cpu().numpy()
     ws = [d[n].cpu().numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    return x, idx, tw, ws
 
-    def sample(n):
-        step = max(1, w.T // n)
-        return step, np.arange(0, w.T, step, dtype=np.int32)[:n]
 
-    _, toks = sample(min(w.T, 64))
+def _sample_note(w, toks, step, n_valid):
+    return (f"{len(toks)} tokens (every {step}th) of the {w.name} workload, {n_valid} valid entries, the same "
+            f"sample in every call; weights of each touched expert dequantised inside the timing")
+
+
+def cpu_baseline(w, d):
+    """The oracle, as it stands, on the host cores: one untimed call, then one
+    timed call on the sample of oracle_sample()."""
+    import oracle
+    oracle.build()
+    x, idx, tw, ws = _oracle_args(d)
+    toks, step = oracle_sample(w)
+    oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
     t0 = time.perf_counter()
     oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
-    t_cal = time.perf_counter() - t0
-    n, dt = len(toks), t_cal
-    for _ in range(3):  # the time grows less than linearly (per-expert weight decoding): refine from the last run
-        if n >= w.T or dt >= 0.7 * target_s:
-            break
-        n = int(min(w.T, max(n + 1, n * target_s / max(dt, 1e-6))))
-        step, toks = sample(n)
-        t0 = time.perf_counter()
-        oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
-        dt = time.perf_counter() - t0
-    step, toks = sample(len(toks))
+    dt = time.perf_counter() - t0
     n_valid = int((idx[toks] >= 0).sum())
     return dict(value=6.0 * n_valid * w.H * w.I / dt / 1e12, unit="TFLOP/s", cores=oracle.num_threads(),
-                kind="oracle", seconds=dt, tokens_per_s=len(toks) / dt,
-                sample=f"{len(toks)} tokens (every {step}th) of the {w.name} workload, {n_valid} valid entries, "
-                       f"weights dequantised per touched expert inside the timing")
+                kind="oracle", seconds=dt, tokens_per_s=len(toks) / dt, sample=_sample_note(w, toks, step, n_valid))
 
 
 def run_reference(args, w, rank, world):
-    """Reference arm: the CPU oracle timed as it stands; rank 0 only."""
+    """Reference arm: the CPU oracle timed as it stands, on rank 0 only; every
+    step is one oracle call on the sample of oracle_sample()."""
     if rank != 0:
         return
-    import numpy as np
     import oracle
     oracle.build()
     d = inputs.make_inputs(w, device="cpu", weight_device="cuda" if torch.cuda.is_available() else "cpu")
-    x = d["x"].view(torch.int16).numpy().view(np.uint16)
-    idx = d["topk_idx"].numpy()
-    tw = d["topk_w"].numpy()
-    ws = [d[n].cpu().numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
-    per_step = max(1, args.ref_tokens)
-    times, flops = [], 0.0
+    x, idx, tw, ws = _oracle_args(d)
+    toks, step = oracle_sample(w)
+    n_valid = int((idx[toks] >= 0).sum())
+    times = []
     for s in range(args.warmup + args.steps):
-        toks = np.unique((np.arange(per_step, dtype=np.int64) * 977 + s * 131) % w.T).astype(np.int32)
         t0 = time.perf_counter()
         oracle.forward(x, idx, tw, w.E, *ws, tokens=toks)
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
-            flops += 6.0 * int((idx[toks] >= 0).sum()) * w.H * w.I
     total = sum(times)
-    value = flops / total / 1e12
+    value = 6.0 * n_valid * w.H * w.I * args.steps / total / 1e12
+    note = _sample_note(w, toks, step, n_valid)
     line = dict(metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
                 ms_per_step=1e3 * total / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="f64", data="synthetic", impl="reference",
-                config=dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}",
-                            sample=f"{per_step} tokens per step"),
+                config=dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}", sample=note),
                 cpu_baseline=dict(value=value, unit="TFLOP/s", cores=oracle.num_threads(), kind="oracle",
-                                  sample=f"{per_step} tokens per step of the {w.name} workload"),
+                                  sample=note),
                 e2e=dict(value=value, unit="TFLOP/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="full", choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU time the cpu_baseline sample aims at")
-    ap.add_argument("--ref-tokens", type=int, default=1, help="oracle tokens per step of the reference arm")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=50)
-    args = ap.parse_args()
-    assert args.warmup >= 3, "at least 3 warm-up steps"
-    w = inputs.WORKLOADS[args.workload]
-    rank, world = dist_init(args)
-    if args.impl == "reference":
-        run_reference(args, w, rank, world)
-        return
+# ------------------------------------------------------------------ GPU legs
+class Layer:
+    """One workload's inputs, prepared weights and workspace on the GPU."""
 
-    import moe_expert_layer_counts_gb300 as moe
-    dev = torch.device("cuda", torch.cuda.current_device())
-    d = inputs.make_inputs(w, seed=0, device=dev)
-    W1 = moe.MXFP4Weight.prepare(d["w1q"], d["w1sf"], layer=1)
-    W2 = moe.MXFP4Weight.prepare(d["w2q"], d["w2sf"], layer=2)
-    ws = moe.alloc_workspace(w.T, w.k, w.E, w.H, w.I, dev)
-    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    n_valid = int((d["topk_idx"] >= 0).sum().item())
-    flops = 6.0 * n_valid * w.H * w.I
-    # weight bytes the step must stream: FP4 codes + UE8M0 scales of every touched expert (W1 and W2)
-    touched = int(torch.unique(d["topk_idx"][d["topk_idx"] >= 0]).numel())
-    weight_bytes = touched * 3 * w.H * w.I * (0.5 + 1.0 / 32)
+    def __init__(self, moe, w, dev):
+        self.moe, self.w = moe, w
+        self.d = inputs.make_inputs(w, seed=0, device=dev)
+        self.W1 = moe.MXFP4Weight.prepare(self.d["w1q"], self.d["w1sf"], layer=1)
+        self.W2 = moe.MXFP4Weight.prepare(self.d["w2q"], self.d["w2sf"], layer=2)
+        self.ws = moe.alloc_workspace(w.T, w.k, w.E, w.H, w.I, dev)
+        self.y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device=dev)
+        idx = self.d["topk_idx"]
+        self.n_valid = int((idx >= 0).sum().item())
+        self.touched = int(torch.unique(idx[idx >= 0]).numel())
+        counts = torch.bincount(idx[idx >= 0].flatten(), minlength=w.E)
+        self.max_count = int(counts.max().item()) if self.n_valid else 0
+        self.flops = 6.0 * self.n_valid * w.H * w.I
+        # FP4 codes + UE8M0 scales of every touched expert (W1 and W2)
+        self.weight_bytes = self.touched * 3 * w.H * w.I * (0.5 + 1.0 / 32)
 
-    def step(ev=None):
+    def step(self, ev=None):
+        m, w, d = self.moe, self.w, self.d
         if ev: ev[0].record()
-        p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I, workspace=ws)
+        p = m.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I, workspace=self.ws)
         if ev: ev[1].record()
-        moe.dispatch(p, d["x"])
+        m.dispatch(p, d["x"])
         if ev: ev[2].record()
-        moe.expert_l1(p, W1)
+        m.expert_l1(p, self.W1)
         if ev: ev[3].record()
-        moe.expert_l2(p, W2)
+        m.expert_l2(p, self.W2)
         if ev: ev[4].record()
-        moe.combine(p, y)
+        m.combine(p, self.y)
         if ev: ev[5].record()
         return p
 
+    def l1_bytes(self):
+        """Algorithmic bytes of one L1 launch: the touched experts' W1 (codes +
+        scales), the pool rows read (codes + scales) and h written."""
+        w = self.w
+        return (self.touched * 2 * w.I * w.H * (0.5 + 1.0 / 32) + self.n_valid * w.H * (1 + 1.0 / 32)
+                + self.n_valid * w.I * (1 + 1.0 / 32))
+
+
+def timed_steps(L, args, world, flush, dev):
+    """W untimed steps, then K steps bracketed by barrier + synchronize, each
+    after an L2 flush (outside the events); CUDA events per stage."""
+    moe = L.moe
     for _ in range(args.warmup):
         flush.fill_(1)
-        p = step()
+        p = L.step()
     torch.cuda.synchronize()
     status = moe.plan_check(p)
     assert status == 0, moe.error_string(status)
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         for i in range(args.steps):
             flush.fill_(i & 255)
-            step(evs[i])
+            p = L.step(evs[i])
         torch.cuda.synchronize()
     barrier(world)
+    status = moe.plan_check(p)
+    assert status == 0, moe.error_string(status)
     stage_ms = {s: 0.0 for s in STAGES}
     total_ms = 0.0
     for e in evs:
@@ -287,16 +300,71 @@ def main():
         for j, s in enumerate(STAGES):
             stage_ms[s] += e[j].elapsed_time(e[j + 1])
     t_max = max_over_ranks(total_ms / 1e3, world)
-    value = world * flops * args.steps / t_max / 1e12
-    ms_step = 1e3 * t_max / args.steps
-    pk = peaks()
-    fp8_sus = 2.0 * pk["bf16_sus"]
-    l1_ms = stage_ms["expert_l1"] / args.steps
-    l1_flops = 4.0 * n_valid * w.H * w.I
-    l1_tf = l1_flops / (l1_ms / 1e3) / 1e12
-    traffic = measured_traffic() if w.name == "full" else None
+    return t_max, {s: v / args.steps for s, v in stage_ms.items()}, clk.summary()
 
-    # end to end through the public API: pinned host inputs -> GPU -> pinned host y
+
+def weight_stream(L, step_s, pk):
+    gbs = L.weight_bytes / step_s / 1e9
+    return dict(touched_experts=L.touched, bytes_per_step=L.weight_bytes, gbs=gbs, pct_hbm=gbs / pk["hbm_gbs"],
+                note=f"touched experts' FP4 + UE8M0 weight bytes per step / step time, vs {pk['source']} "
+                     f"HBM copy bandwidth {pk['hbm_gbs']} GB/s")
+
+
+def roofline(L, stage_ms, pk, mma):
+    """The dominant kernel, L1: tensor-bound against the FP8 peak (and the
+    measured block-scaled MMA ceiling) when experts hold more than 16 rows,
+    otherwise bound by its weight stream from HBM."""
+    w = L.w
+    l1_s = stage_ms["expert_l1"] / 1e3
+    if L.max_count <= 16:
+        gb = L.l1_bytes()
+        ach = gb / l1_s / 1e9
+        return dict(kernel="expert_gemm_kernel<1> (L1)", bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s",
+                    frac=ach / pk["hbm_gbs"], traffic=measured_traffic(w.name),
+                    algorithmic=f"touched W1 (codes + scales) + pool rows read + h written = {gb:.4g} B per launch",
+                    peak_note=f"{pk['source']} HBM copy bandwidth")
+    fl = 4.0 * L.n_valid * w.H * w.I
+    ach = fl / l1_s / 1e12
+    fp8 = 2.0 * pk["bf16"]
+    r = dict(kernel="expert_gemm_kernel<1> (L1)", bound="tensor", achieved=ach, peak=fp8, unit="TFLOP/s",
+             frac=ach / fp8, traffic=measured_traffic(w.name),
+             algorithmic=f"4*N*H*I = {fl:.4g} FLOP per launch (valid rows only)",
+             peak_note=f"FP8 = 2 x {pk['source']} burst bf16 cuBLAS rate ({pk['bf16']} TF/s), the nominal FP8/bf16 "
+                       f"ratio of the dense tensor rates")
+    if mma:
+        r.update(frac_vs_mma=ach / mma["tflops"], mma_ceiling_tflops=mma["tflops"])
+    return r
+
+
+def mma_ceiling(moe):
+    """The block-scaled MMA (the GEMMs' instruction) issued back to back on every
+    SM from fixed shared-memory operands: the tensor pipe's rate on this GPU."""
+    tflops, ctas, ms = moe.selftest_mma_rate(kblocks=16384, repeats=3)
+    return dict(tflops=tflops, ctas=ctas, ms=ms,
+                note="moe_selftest_mma_rate: M=128 N=256 K=32 kind::mxf8f6f4 block-scaled MMAs, one CTA per SM, "
+                     "16384 x 4 per CTA, best of 3 launches")
+
+
+def decode_leg(moe, args, world, flush, dev, pk):
+    """The decode-shaped workload, timed like the main one."""
+    w = inputs.WORKLOADS["decode"]
+    L = Layer(moe, w, dev)
+    t, stage_ms, clk = timed_steps(L, args, world, flush, dev)
+    step_s = t / args.steps
+    out = dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}", ms_per_step=1e3 * step_s,
+               value=world * L.flops / step_s / 1e12, unit="TFLOP/s", tokens_per_s=world * w.T / step_s,
+               stage_ms=stage_ms, weight_stream=weight_stream(L, step_s, pk), roofline=roofline(L, stage_ms, pk, None),
+               clocks=clk, gpu_launches=kernels_per_step(w) * args.steps)
+    del L
+    torch.cuda.empty_cache()
+    return out
+
+
+def e2e_legs(L, args, world, flush):
+    """End to end through the public API: pinned host inputs -> GPU -> pinned
+    host y, three ways (a pipelined stream of steps, one step at a time, one
+    step as a replayed CUDA graph)."""
+    moe, w, d = L.moe, L.w, L.d
     hx = d["x"].cpu().pin_memory()
     hidx = d["topk_idx"].cpu().pin_memory()
     htw = d["topk_w"].cpu().pin_memory()
@@ -310,17 +378,16 @@ def main():
         gx.copy_(hx, non_blocking=True)
         gidx.copy_(hidx, non_blocking=True)
         gtw.copy_(htw, non_blocking=True)
-        pp = moe.plan(gidx, gtw, w.E, w.H, w.I, workspace=ws)
-        moe.forward(gx, W1, W2, pp, y)
-        hy.copy_(y, non_blocking=True)
+        pp = moe.plan(gidx, gtw, w.E, w.H, w.I, workspace=L.ws)
+        moe.forward(gx, L.W1, L.W2, pp, L.y)
+        hy.copy_(L.y, non_blocking=True)
         b.record()
         b.synchronize()
         if i >= args.warmup:
             e2e_ms += a.elapsed_time(b)
     e2e_t = max_over_ranks(e2e_ms / 1e3, world)
-    e2e_val = world * flops * args.e2e_steps / e2e_t / 1e12
+    serial = world * L.flops * args.e2e_steps / e2e_t / 1e12
 
-    # the same step captured once in a CUDA graph (copies in, plan, forward, copy out) and replayed
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
@@ -329,9 +396,9 @@ def main():
             gx.copy_(hx, non_blocking=True)
             gidx.copy_(hidx, non_blocking=True)
             gtw.copy_(htw, non_blocking=True)
-            gp = moe.plan(gidx, gtw, w.E, w.H, w.I, workspace=ws)
-            moe.forward(gx, W1, W2, gp, y)
-            hy.copy_(y, non_blocking=True)
+            gp = moe.plan(gidx, gtw, w.E, w.H, w.I, workspace=L.ws)
+            moe.forward(gx, L.W1, L.W2, gp, L.y)
+            hy.copy_(L.y, non_blocking=True)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     graph_ms = 0.0
@@ -347,7 +414,7 @@ def main():
     status = moe.plan_check(gp)
     assert status == 0, moe.error_string(status)
     graph_t = max_over_ranks(graph_ms / 1e3, world)
-    graph_val = world * flops * args.e2e_steps / graph_t / 1e12
+    graph_val = world * L.flops * args.e2e_steps / graph_t / 1e12
     # a stream of steps as a serving loop runs them: copies in, compute and copies out on three streams, two
     # buffer sets, so step i+1's inputs arrive and step i-1's output leaves while step i computes (every step's
     # copies stay inside the timed region; no L2 flush: the weights and the pool exceed L2 on these workloads)
@@ -378,8 +445,8 @@ def main():
             s_comp.wait_event(ev_in)
             if i >= 2:
                 s_comp.wait_event(ev_out[b])
-            pl = moe.plan(gidx2[b], gtw2[b], w.E, w.H, w.I, workspace=ws, stream=s_comp)
-            moe.forward(gx2[b], W1, W2, pl, y2[b], stream=s_comp)
+            pl = moe.plan(gidx2[b], gtw2[b], w.E, w.H, w.I, workspace=L.ws, stream=s_comp)
+            moe.forward(gx2[b], L.W1, L.W2, pl, y2[b], stream=s_comp)
             ev_comp[b].record(s_comp)
             s_out.wait_event(ev_comp[b])
             with torch.cuda.stream(s_out):
@@ -395,49 +462,78 @@ def main():
     status = moe.plan_check(pl, stream=s_comp)
     assert status == 0, moe.error_string(status)
     pipe_t = max_over_ranks(pipe_ms / 1e3, world)
-    pipe_val = world * flops * args.e2e_steps / pipe_t / 1e12
+    pipe_val = world * L.flops * args.e2e_steps / pipe_t / 1e12
     h2d = hx.numel() * 2 + hidx.numel() * 8 + htw.numel() * 4
     d2h = hy.numel() * 2
+    return dict(value=pipe_val, unit="TFLOP/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                ms_per_step=1e3 * pipe_t / args.e2e_steps,
+                note="a stream of steps through the public API: each step copies its inputs in from pinned host "
+                     "memory and its y out; copies in, compute and copies out run on three streams with two "
+                     "buffer sets, so the copies of neighbouring steps overlap the compute",
+                serial=dict(value=serial, unit="TFLOP/s", ms_per_step=1e3 * e2e_t / args.e2e_steps,
+                            note="one step at a time: copy in, plan, forward, copy out, wait"),
+                graph=dict(value=graph_val, unit="TFLOP/s", ms_per_step=1e3 * graph_t / args.e2e_steps,
+                           note="one step at a time, captured once in a CUDA graph and replayed"))
 
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="full", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode leg of the default run")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    w = inputs.WORKLOADS[args.workload]
+    rank, world = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import moe_expert_layer_counts_gb300 as moe
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk = peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    mma = mma_ceiling(moe)
+    L = Layer(moe, w, dev)
+    t_max, stage_ms, clk = timed_steps(L, args, world, flush, dev)
+    value = world * L.flops * args.steps / t_max / 1e12
+    step_s = t_max / args.steps
+    e2e = e2e_legs(L, args, world, flush)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, d, args.cpu_seconds)
-    if rank != 0:
-        return
+        cpu = cpu_baseline(w, L.d)
+    fp8 = 2.0 * pk["bf16"]
     line = dict(
         metric=METRIC, value=value, unit="TFLOP/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
-        ms_per_step=ms_step, higher_is_better=True, scaling="weak", vs_baseline=None,
+        ms_per_step=1e3 * step_s, higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="e4m3 x e2m1 -> fp32 (MXFP8 x MXFP4, UE8M0/32)", data="synthetic",
         config=dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}", T=w.T, H=w.H, I=w.I, E=w.E,
-                    k=w.k, valid_entries=n_valid, l2="flushed before every timed step (512 MB write)",
+                    k=w.k, valid_entries=L.n_valid, l2="flushed before every timed step (512 MB write)",
                     parallelism=f"replicas x{world}"),
-        tokens_per_s=world * w.T * args.steps / t_max,
-        weight_stream=dict(touched_experts=touched, bytes_per_step=weight_bytes,
-                           gbs=weight_bytes / (t_max / args.steps) / 1e9,
-                           pct_hbm=weight_bytes / (t_max / args.steps) / 1e9 / pk["hbm_gbs"],
-                           note=f"touched experts' FP4 + UE8M0 weight bytes per step / step time, vs {pk['source']} "
-                                f"HBM copy bandwidth {pk['hbm_gbs']} GB/s"),
-        pct_fp8_peak=value / fp8_sus,
-        fp8_peak_tflops=dict(value=fp8_sus, note=f"2 x {pk['source']} sustained bf16 cuBLAS rate"),
-        stage_ms={s: v / args.steps for s, v in stage_ms.items()},
-        roofline=dict(kernel="expert_gemm_kernel<1> (L1)", bound="tensor", achieved=l1_tf, peak=fp8_sus,
-                      unit="TFLOP/s", frac=l1_tf / fp8_sus, traffic=traffic,
-                      algorithmic=f"4*N*H*I = {l1_flops:.4g} FLOP per launch (valid rows only)",
-                      peak_note=f"FP8 = 2 x {pk['source']} sustained bf16 ({pk['bf16_sus']} TF/s)"),
-        e2e=dict(value=pipe_val, unit="TFLOP/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                 ms_per_step=1e3 * pipe_t / args.e2e_steps,
-                 note="a stream of steps through the public API: each step copies its inputs in from pinned host "
-                      "memory and its y out; copies in, compute and copies out run on three streams with two "
-                      "buffer sets, so the copies of neighbouring steps overlap the compute",
-                 serial=dict(value=e2e_val, unit="TFLOP/s", ms_per_step=1e3 * e2e_t / args.e2e_steps,
-                             note="one step at a time: copy in, plan, forward, copy out, wait"),
-                 graph=dict(value=graph_val, unit="TFLOP/s", ms_per_step=1e3 * graph_t / args.e2e_steps,
-                            note="one step at a time, captured once in a CUDA graph and replayed")),
+        tokens_per_s=world * w.T / step_s,
+        weight_stream=weight_stream(L, step_s, pk),
+        pct_fp8_peak=value / world / fp8,
+        fp8_peak_tflops=dict(value=fp8, note=f"2 x {pk['source']} burst bf16 cuBLAS rate ({pk['bf16']} TF/s)"),
+        pct_mma_ceiling=value / world / mma["tflops"],
+        mma_ceiling=mma,
+        stage_ms=stage_ms,
+        roofline=roofline(L, stage_ms, pk, mma),
+        e2e=e2e,
         gpu_launches=kernels_per_step(w) * args.steps,
-        clocks=clk.summary(),
+        clocks=clk,
         cpu_baseline=cpu,
     )
-    print(json.dumps(line), flush=True)
+    del L, e2e
+    torch.cuda.empty_cache()
+    if w.name != "decode" and not args.no_decode:
+        line["decode"] = decode_leg(moe, args, world, flush, dev, pk)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -238,10 +238,14 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
  * Limits: T*k <= 262144, E <= 1024, ceil(T*k / 2048) * E <= 32768, 1 <= k <= 32;
  * larger sizes return MOE_ERR_TOO_LARGE before anything is enqueued.
  * The first call on a device looks up the array's device address (a CUDA
- * runtime query, no allocation); make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
- * contents, so calls whose kernels overlap on the GPU (different streams
- * without ordering) race and give wrong results; order them on one stream. */
+ * runtime query, no allocation) and keeps it for the life of the process;
+ * make that first call before any stream capture, and do not call this entry
+ * point on a device again after cudaDeviceReset() on it (the kept address
+ * would belong to the destroyed context).  Concurrent first calls from
+ * several host threads are safe.  All calls share the one array and it keeps
+ * the last call's contents, so calls whose kernels overlap on the GPU
+ * (different streams without ordering) race and give wrong results; order
+ * them on one stream. */
 int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, int E, int32_t* count, int32_t* offsets,
                               int32_t* padded_offsets, void* stream);
 
@@ -256,6 +260,21 @@ int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, int E, int3
  * MOE_ERR_UNSUPPORTED (not an sm_103 device), MOE_ERR_CUDA.  The kernel never
  * traps; after a time-out the context stays usable. */
 int moe_selftest_bounded_wait(int arrive, uint64_t timeout_ns, int32_t* out, void* stream);
+
+/* Tensor-pipe ceiling of the block-scaled MMA that the expert GEMMs issue
+ * (no counterpart on the pages; a calibration for the roofline of the GEMMs).
+ * Launches one CTA per SM; in each, one thread issues kblocks x 4
+ * tcgen05.mma.kind::mxf8f6f4.block_scale instructions (M = 128, N = 256,
+ * K = 32: E4M3 x E2M1 with UE8M0 scales, the GEMMs' instruction) back to back
+ * on fixed shared-memory operands, then waits for them.  No global memory is
+ * touched except `status`.  The caller times the launch (e.g. CUDA events on
+ * `stream`): the work is ctas * kblocks * 2*128*256*128 FLOP.
+ *   kblocks  1 .. 2^20 (about 260 ns each per SM at the full tensor rate)
+ *   status   device int32, written: MOE_OK, or MOE_ERR_TIMEOUT if the MMAs did
+ *            not complete within 2 s of global time
+ *   ctas     out (host): the number of CTAs launched (the SM count)
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (not sm_103), MOE_ERR_CUDA. */
+int moe_selftest_mma_rate(int kblocks, int32_t* status, int* ctas, void* stream);
 
 /* Static text for a status code. */
 const char* moe_error_string(int status);

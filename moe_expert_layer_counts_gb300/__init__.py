@@ -48,7 +48,8 @@ _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_
 # every function declared in include/moe.h
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",
            "moe_dispatch", "moe_expert_l1", "moe_expert_l2", "moe_combine", "moe_forward", "moe_plan_check",
-           "moe_plan_export", "moe_error_string", "moe_expert_offsets_static", "moe_selftest_bounded_wait")
+           "moe_plan_export", "moe_error_string", "moe_expert_offsets_static", "moe_selftest_bounded_wait",
+           "moe_selftest_mma_rate")
 
 
 class MoeError(RuntimeError):
@@ -124,6 +125,8 @@ def lib():
             L.moe_expert_offsets_static.argtypes = [P, i32, i32, i32, P, P, P, P]
             L.moe_selftest_bounded_wait.restype = i32
             L.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint64, P, P]
+            L.moe_selftest_mma_rate.restype = i32
+            L.moe_selftest_mma_rate.argtypes = [i32, P, ctypes.POINTER(i32), P]
             L.moe_error_string.restype = ctypes.c_char_p
             L.moe_error_string.argtypes = [i32]
             _lib = L
@@ -286,3 +289,28 @@ def selftest_bounded_wait(arrive: bool, timeout_ns: int, stream=None):
     torch.cuda.synchronize()
     st, us = (int(v) for v in out.cpu())
     return st, us
+
+
+MMA_FLOP_PER_KBLOCK = 4 * 2 * 128 * 256 * 32
+
+
+def selftest_mma_rate(kblocks: int = 16384, repeats: int = 3, stream=None):
+    """moe_selftest_mma_rate timed with CUDA events: the best of `repeats`
+    launches (after one warm-up), as (TFLOP/s, CTAs, ms per launch)."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream() if stream is None else stream
+    ctas = ctypes.c_int(0)
+    best = None
+    for i in range(repeats + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        _check(lib().moe_selftest_mma_rate(int(kblocks), _ptr(status), ctypes.byref(ctas),
+                                           ctypes.c_void_p(s.cuda_stream)), "moe_selftest_mma_rate")
+        b.record(s)
+        b.synchronize()
+        _check(int(status.item()), "moe_selftest_mma_rate (device)")
+        if i > 0:
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+    tflops = ctas.value * kblocks * MMA_FLOP_PER_KBLOCK / (best / 1e3) / 1e12
+    return tflops, ctas.value, best

@@ -326,6 +326,15 @@ int moe_selftest_bounded_wait(int arrive, uint64_t timeout_ns, int32_t* out, voi
     return cuda_status(launch_bounded_wait_selftest(arrive, timeout_ns, out, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_selftest_mma_rate(int kblocks, int32_t* status, int* ctas, void* stream) {
+    if (!status || !ctas || kblocks < 1 || kblocks > (1 << 20)) return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = device_info(&sms);
+    if (rc) return rc;
+    *ctas = sms;
+    return cuda_status(launch_mma_rate_selftest(kblocks, sms, status, static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_error_string(int status) {
     switch (status) {
         case MOE_OK: return "ok";

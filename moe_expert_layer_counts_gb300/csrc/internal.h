@@ -54,6 +54,7 @@ cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves
                               cudaStream_t s);
 
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t timeout_ns, int32_t* out, cudaStream_t s);
+cudaError_t launch_mma_rate_selftest(int kblocks, int ctas, int32_t* status, cudaStream_t s);
 
 struct GemmLaunch {
     const void* w_q;      // packed e2m1 weights [E, N, K/2]

@@ -25,6 +25,8 @@
 // single launch.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 namespace moe {
@@ -415,15 +417,24 @@ constexpr int kStaticInts = kStaticErr + 32;
 
 static __device__ __align__(256) int g_offsets_scratch[kStaticInts];
 
+// Device address of the array on device `dev` (which must be current),
+// looked up on the first call for that device and cached.  The cache is one
+// atomic pointer per device: two host threads that make the first call at
+// the same time both look the address up and store the same value.  A cached
+// address belongs to the context it was looked up in; after cudaDeviceReset()
+// it is stale, so the entry point must not be called on that device again in
+// the same process (stated in moe.h).
+std::atomic<int*> g_static_ptrs[64];
+
 int* static_scratch_ptr(int dev) {
-    static int* ptrs[64] = {};
     if (dev < 0 || dev >= 64) return nullptr;
-    if (!ptrs[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_offsets_scratch) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<int*>(p);
-    }
-    return ptrs[dev];
+    int* p = g_static_ptrs[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_offsets_scratch) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(a);
+    g_static_ptrs[dev].store(p, std::memory_order_release);
+    return p;
 }
 
 }  // namespace
@@ -447,9 +458,10 @@ extern "C" int moe_expert_offsets_static(const int64_t* topk_idx, int T, int k, 
     int* scratch = static_scratch_ptr(dev);
     if (!scratch) return MOE_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the error word is the only scratch that must start at zero; the count
-    // and scan kernels overwrite every other word they read
-    if (cudaMemsetAsync(scratch + kStaticErr, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // Nothing needs clearing: the count kernel writes every histogram cell the
+    // scan reads, and the scan writes every base and table cell.  The count
+    // kernel's bad-id flag lands in a word that nothing reads (this entry point
+    // skips ids outside [-1, E) without reporting them).
     if (chunks > 0) {
         route_count_kernel<<<chunks, kCountThreads, E * sizeof(int), s>>>(topk_idx, n, E, scratch + kStaticHist,
                                                                           scratch + kStaticErr);

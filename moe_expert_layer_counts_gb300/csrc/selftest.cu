@@ -36,7 +36,96 @@ __global__ void __launch_bounds__(64) bounded_wait_kernel(int arrive, uint64_t t
 #endif
 }
 
+// Tensor-pipe ceiling of the block-scaled MMA the expert GEMMs issue: one CTA
+// per SM (the shared-memory request keeps a second one off the SM), one
+// thread issuing `kblocks` x 4 tcgen05.mma.kind::mxf8f6f4.block_scale (M = 128,
+// N = 256, K = 32, E4M3 x E2M1, UE8M0 scales) back to back on fixed
+// shared-memory operands into one tensor-memory accumulator, then waiting
+// (bounded) for them to complete.  The operands are a fixed pseudo-random
+// pattern; nothing is read from or written to global memory except the
+// status word.
+constexpr int kRateABytes = 16384, kRateBBytes = 32768, kRateSfBytes = 1536;
+constexpr int kRateSmem = 120 * 1024;  // above half of the SM's shared memory: one CTA per SM
+
+__global__ void __launch_bounds__(64, 1) mma_rate_kernel(int kblocks, int32_t* status) {
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
+    extern __shared__ uint8_t raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t tbase;
+    // operands: a fixed pseudo-random byte pattern (finite E4M3 codes: bit 3 of
+    // every byte cleared, so no byte is 0x7F or 0xFF), so that the tensor pipe
+    // switches as it does on real data; scale bytes 127 (2^0)
+    for (int i = threadIdx.x; i < (kRateABytes + kRateBBytes) / 4; i += blockDim.x) {
+        uint32_t h = static_cast<uint32_t>(i) * 2654435761u + blockIdx.x * 40503u;
+        h ^= h >> 15;
+        h *= 2246822519u;
+        h ^= h >> 13;
+        reinterpret_cast<uint32_t*>(smem)[i] = h & 0xF7F7F7F7u;
+    }
+    for (int i = threadIdx.x; i < kRateSfBytes; i += blockDim.x) smem[kRateABytes + kRateBBytes + i] = 127;
+    ptx::fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bar), 1);
+        ptx::fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        ptx::tmem_alloc(ptx::smem_addr(&tbase), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&tbase);
+    if (threadIdx.x == 32) {
+        const uint32_t s0 = ptx::smem_addr(smem);
+        const uint64_t sf = ptx::desc_sf_32x16(s0 + kRateABytes + kRateBBytes);
+        ptx::tc_cp_32x128b_warpx4(tmem + 256, sf);
+        ptx::tc_cp_32x128b_warpx4(tmem + 260, sf + (512 >> 4));
+        ptx::tc_cp_32x128b_warpx4(tmem + 264, sf + (1024 >> 4));
+        const uint64_t a = ptx::desc_kmajor_sw128(s0), b = ptx::desc_kmajor_sw128(s0 + kRateABytes);
+        constexpr uint32_t idesc = ptx::idesc_e4m3_e2m1(128, 256);
+        for (int kb = 0; kb < kblocks; ++kb) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_mxf8f6f4(tmem, a + 2 * kk, b + 2 * kk, ptx::idesc_with_sf_id(idesc, kk), tmem + 256,
+                                  tmem + 260, (kb | kk) != 0);
+        }
+        ptx::tc_commit(ptx::smem_addr(&bar));
+        if (!ptx::mbar_wait(ptx::smem_addr(&bar), 0, ptx::globaltimer() + 2000000000ull)) {
+            atomicExch(status, MOE_ERR_TIMEOUT);
+            // the accumulator must not be freed under running MMAs: wait once more, bounded
+            ptx::mbar_wait(ptx::smem_addr(&bar), 0, ptx::globaltimer() + 2000000000ull);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+#else
+    if (threadIdx.x == 0 && blockIdx.x == 0) *status = MOE_ERR_NO_KERNEL;
+#endif
+}
+
 }  // namespace
+
+cudaError_t launch_mma_rate_selftest(int kblocks, int ctas, int32_t* status, cudaStream_t s) {
+    static int attr_done[64] = {};
+    int dev = 0;
+    cudaError_t st = cudaGetDevice(&dev);
+    if (st != cudaSuccess) return st;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev]) {
+        st = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);
+        if (st != cudaSuccess) return st;
+        attr_done[dev] = 1;
+    }
+    if ((st = cudaMemsetAsync(status, 0, sizeof(int32_t), s)) != cudaSuccess) return st;
+    mma_rate_kernel<<<ctas, 64, kRateSmem, s>>>(kblocks, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t timeout_ns, int32_t* out, cudaStream_t s) {
     bounded_wait_kernel<<<1, 64, 0, s>>>(arrive, timeout_ns, out);

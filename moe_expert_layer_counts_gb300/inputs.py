@@ -1,10 +1,10 @@
 """Seeded synthetic inputs for the fused MoE forward.
 
 This module is shared by the tests and the benchmark.  It holds none of the
-layer's arithmetic: it draws random numbers and runs a harness router
-(softmax -> top-k -> renormalise, which is not part of the layer).  The FP4
-weights are drawn directly in their quantised form, as random E2M1 codes and
-random UE8M0 exponents, so no quantiser lives here.
+layer's arithmetic: it draws random numbers, runs a harness router (softmax
+-> top-k -> renormalise, which is not part of the layer) and turns Gaussian
+weights into the MXFP4 bytes the layer takes as input (the layer never
+quantises weights; this is how its inputs are made).
 
 Workloads (all seeded, seed 0):
   tiny    T=64,   H=256,  I=128,  E=8,   k=2, uniform router
@@ -15,12 +15,14 @@ Workloads (all seeded, seed 0):
           per-expert bias (load imbalance)
   decode  T=128,  H=7168, I=2048, E=256, k=8, uniform router
 
-x ~ N(0,1) cast to bf16.  Weights W1 [E,2I,H], W2 [E,H,I] have the
-distribution of N(0, 1/sqrt(K)) quantised to MXFP4 (one UE8M0 per 32 along
-K): each E2M1 magnitude index is drawn from the probabilities that |2z|,
-z ~ N(0,1), lies nearest to that E2M1 magnitude, the sign is a fair coin,
-and each 32-block's exponent is s0 or s0+1 with the probability that makes
-E[w^2] = 1/K.
+x ~ N(0,1) cast to bf16.  Weights W1 [E,2I,H], W2 [E,H,I] are drawn as
+N(0, 1/sqrt(K)) (standard deviation 1/sqrt(K), K the reduction length) and
+quantised to MXFP4 along K, one expert at a time on the weights' device: per
+32-block the UE8M0 scale 2^e with the smallest e such that amax <= 6 * 2^e
+(clamped to [-126, 127], 2^0 for an all-zero block), then every value / 2^e
+rounded to the nearest E2M1 value (0, .5, 1, 1.5, 2, 3, 4, 6), ties to the
+even code, sign in bit 3.  Codes are packed two per byte, the even K index in
+the low nibble.
 """
 from __future__ import annotations
 
@@ -30,7 +32,6 @@ from dataclasses import dataclass
 import torch
 
 SF_VEC = 32
-_E2M1_MAG = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
 
 
 @dataclass(frozen=True)
@@ -89,43 +90,47 @@ def make_routing(w: Workload, seed: int = 1, device="cpu"):
     return topi.to(torch.int64).contiguous(), topw.to(torch.float32).contiguous()
 
 
-def _e2m1_magnitude_probs():
-    """P(|2z| nearest to each E2M1 magnitude), z ~ N(0,1), and E[v^2]."""
-    edges = [0.0] + [(a + b) / 2 for a, b in zip(_E2M1_MAG[:-1], _E2M1_MAG[1:])] + [math.inf]
-    cdf = [math.erf((e / 2.0) / math.sqrt(2.0)) if e != math.inf else 1.0 for e in edges]
-    probs = [cdf[i + 1] - cdf[i] for i in range(8)]
-    ev2 = sum(p * m * m for p, m in zip(probs, _E2M1_MAG))
-    return probs, ev2
+# midpoints between consecutive E2M1 magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6
+_E2M1_MIDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
 
 
-def weight_exponent_recipe(K: int):
-    """(s0, p_up): each 32-block exponent is s0+1 with probability p_up, else s0,
-    so that E[w^2] = 1/K for w = v * 2^s."""
-    _, ev2 = _e2m1_magnitude_probs()
-    target = 1.0 / K
-    s0 = math.floor(0.5 * math.log2(target / ev2))
-    p_up = (target / (ev2 * 4.0 ** s0) - 1.0) / 3.0
-    return s0, min(max(p_up, 0.0), 1.0)
+def quantize_mxfp4(w: torch.Tensor):
+    """MXFP4 bytes of a float tensor [N, K] (K a multiple of 32): (q uint8
+    [N, K/2], sf uint8 [N, K/32] biased exponents), by the rule in the module
+    docstring.  The scale exponent is read off frexp(amax) = f * 2^q (f in
+    [0.5, 1)): 6 * 2^e >= amax first holds at e = q - 3 when f <= 0.75 and at
+    e = q - 2 otherwise; both comparisons are exact."""
+    N, K = w.shape
+    assert K % SF_VEC == 0
+    b = w.to(torch.float64).reshape(N, K // SF_VEC, SF_VEC)
+    amax = b.abs().amax(dim=-1)
+    f, q = torch.frexp(amax)
+    e = torch.where(f <= 0.75, q - 3, q - 2)
+    e = torch.where(amax > 0, e, torch.zeros_like(e)).clamp(-126, 127)
+    v = b * torch.exp2(-e.to(torch.float64))[..., None]
+    a = v.abs()
+    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float64, device=w.device)
+    code = torch.bucketize(a, mids, right=False)          # midpoints strictly below a
+    tie = (code < len(_E2M1_MIDS)) & (a == mids[code.clamp(max=len(_E2M1_MIDS) - 1)])
+    code = code + (tie & (code % 2 == 1)).to(code.dtype)   # a tie goes to the even code
+    neg = (v < 0) | ((v == 0) & torch.signbit(v))
+    nib = (code | (neg.to(code.dtype) << 3)).to(torch.uint8).reshape(N, K)
+    qb = nib[:, 0::2] | (nib[:, 1::2] << 4)
+    return qb.contiguous(), (e + 127).to(torch.uint8).contiguous()
 
 
 def make_weights(E: int, N: int, K: int, seed: int, device="cpu"):
-    """MXFP4 weights [E,N,K]: (q uint8 [E,N,K/2], two codes per byte with the
-    even K index in the low nibble; sf uint8 [E,N,K/32], biased exponents)."""
+    """MXFP4 weights [E,N,K] quantised from N(0, 1/sqrt(K)): (q uint8
+    [E,N,K/2], two codes per byte with the even K index in the low nibble;
+    sf uint8 [E,N,K/32], biased exponents)."""
     assert K % SF_VEC == 0
     g = _gen(seed, device)
-    probs, _ = _e2m1_magnitude_probs()
-    cum = torch.tensor([sum(probs[: i + 1]) for i in range(7)], device=device, dtype=torch.float32)
-    s0, p_up = weight_exponent_recipe(K)
     q = torch.empty(E, N, K // 2, dtype=torch.uint8, device=device)
     sf = torch.empty(E, N, K // SF_VEC, dtype=torch.uint8, device=device)
+    std = 1.0 / math.sqrt(K)
     for e in range(E):
-        u = torch.rand(N, K, generator=g, device=device, dtype=torch.float32)
-        mag = torch.bucketize(u, cum, right=True).to(torch.uint8)  # 0..7
-        sign = (torch.rand(N, K, generator=g, device=device) < 0.5).to(torch.uint8) << 3
-        nib = mag | sign
-        q[e] = nib[:, 0::2] | (nib[:, 1::2] << 4)
-        up = (torch.rand(N, K // SF_VEC, generator=g, device=device) < p_up).to(torch.uint8)
-        sf[e] = (127 + s0) + up
+        w = torch.randn(N, K, generator=g, device=device, dtype=torch.float32) * std
+        q[e], sf[e] = quantize_mxfp4(w)
     return q, sf
 
 

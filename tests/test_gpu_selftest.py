@@ -33,3 +33,13 @@ def test_bounded_wait_argument_checks(moe):
     for args in ((True, 0), (True, 3_000_000_000)):
         with pytest.raises(moe.MoeError):
             moe.selftest_bounded_wait(*args)
+
+
+def test_mma_rate_calibration(moe):
+    """The block-scaled MMA ceiling kernel completes (status OK) on every SM and
+    reports a rate in the plausible band of this GPU's FP8 tensor pipe."""
+    tflops, ctas, ms = moe.selftest_mma_rate(kblocks=2048, repeats=1)
+    assert ctas >= 100
+    assert 1000.0 < tflops < 20000.0, tflops
+    with pytest.raises(moe.MoeError):
+        moe.selftest_mma_rate(kblocks=0)

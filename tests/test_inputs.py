@@ -6,21 +6,47 @@ from moe_expert_layer_counts_gb300 import inputs
 
 
 def test_weights_distribution(oracle):
-    K = 2048
-    q, sf = inputs.make_weights(2, 64, K, seed=0)
-    assert q.shape == (2, 64, K // 2) and sf.shape == (2, 64, K // 32)
+    """Gaussian weights N(0, 1/sqrt(K)) quantised to MXFP4: the bytes equal the
+    oracle's own MX E2M1 quantiser (an independent implementation) applied to
+    the same Gaussian draw, the dequantised weights have the configured
+    spread, and every 32-block's largest magnitude maps to code 5, 6 or 7 (a
+    value in (3, 6] after the ceil scale rule)."""
+    K, N, E = 2048, 64, 2
+    q, sf = inputs.make_weights(E, N, K, seed=0)
+    assert q.shape == (E, N, K // 2) and sf.shape == (E, N, K // 32)
+    g = torch.Generator().manual_seed(0)
+    for e in range(E):
+        w = torch.randn(N, K, generator=g, dtype=torch.float32) / np.sqrt(K)
+        nib, osf = oracle.quant_mx_e2m1(w.numpy())
+        packed = nib.reshape(N, K)[:, 0::2] | (nib.reshape(N, K)[:, 1::2] << 4)
+        np.testing.assert_array_equal(q[e].numpy(), packed)
+        np.testing.assert_array_equal(sf[e].numpy().ravel(), osf)
     tab = np.array([oracle.e2m1_decode(c) for c in range(16)])
     qn = q.numpy()
-    nib = np.stack([qn & 15, qn >> 4], -1).reshape(2, 64, K)
+    nib = np.stack([qn & 15, qn >> 4], -1).reshape(E, N, K)
     scale = np.exp2(sf.numpy().astype(np.float64) - 127).repeat(32, -1)
-    w = tab[nib] * scale
-    assert abs(w.std() * np.sqrt(K) - 1.0) < 0.05, w.std() * np.sqrt(K)
-    assert abs(w.mean()) < 0.05 / np.sqrt(K)
-    s0, p_up = inputs.weight_exponent_recipe(K)
-    assert set(np.unique(sf.numpy())) <= {127 + s0, 128 + s0}
+    wq = tab[nib] * scale
+    assert abs(wq.std() * np.sqrt(K) - 1.0) < 0.05, wq.std() * np.sqrt(K)
+    assert abs(wq.mean()) < 0.05 / np.sqrt(K)
+    top = (nib & 7).reshape(E, N, K // 32, 32).max(-1)
+    assert top.min() >= 5
     # same seed, same bytes
-    q2, sf2 = inputs.make_weights(2, 64, K, seed=0)
+    q2, sf2 = inputs.make_weights(E, N, K, seed=0)
     assert torch.equal(q, q2) and torch.equal(sf, sf2)
+
+
+def test_quantize_mxfp4_ties_and_signs(oracle):
+    """Rounding ties go to the even E2M1 code, negative values (and a value
+    that rounds to zero from below) carry the sign bit, an all-zero block has
+    scale byte 127: the same bytes as the oracle's codec."""
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0], np.float32)
+    row = np.concatenate([ties, -ties, np.array([-0.1, 0.1, 0.0, -0.0] + [0.0] * 12, np.float32)])
+    w = torch.from_numpy(np.stack([row, np.zeros(32, np.float32)]))
+    q, sf = inputs.quantize_mxfp4(w)
+    nib, osf = oracle.quant_mx_e2m1(w.numpy())
+    np.testing.assert_array_equal(q.numpy(), (nib.reshape(2, 32)[:, 0::2] | (nib.reshape(2, 32)[:, 1::2] << 4)))
+    np.testing.assert_array_equal(sf.numpy().ravel(), osf)
+    assert sf[1, 0] == 127
 
 
 def test_routing_workloads():

@@ -55,6 +55,35 @@ def test_offsets_static_matches_plan_on_consecutive_calls(moe):
         np.testing.assert_array_equal(g, r)
 
 
+def _oracle_tables(oracle, idx_np, E):
+    r = oracle.plan(idx_np, np.ones(idx_np.shape, np.float32), E)
+    return r["count"], r["off"], r["poff"]
+
+
+def test_offsets_static_edge_cases_against_oracle(moe, oracle):
+    """Edge cases, compared directly with the oracle's plan (which skips every
+    id outside [0, E)): an empty batch, one expert, ids of -1 and ids out of
+    range (skipped here without a report), a single entry, and a batch that
+    fits one routing chunk next to one that needs several."""
+    rng = np.random.default_rng(17)
+    cases = []
+    cases.append(("T=0", np.zeros((0, 4), np.int64), 8))
+    cases.append(("E=1", np.zeros((300, 2), np.int64), 1))
+    bad = rng.integers(0, 16, (500, 3)).astype(np.int64)
+    bad[rng.random(bad.shape) < 0.2] = -1
+    bad[3, 1], bad[77, 0], bad[400, 2] = 16, -2, 1 << 40
+    cases.append(("bad ids", bad, 16))
+    cases.append(("one entry", np.array([[5]], np.int64), 6))
+    cases.append(("one chunk", rng.integers(0, 40, (256, 8)).astype(np.int64), 40))
+    cases.append(("many chunks", rng.integers(-1, 300, (4000, 6)).astype(np.int64), 300))
+    for name, idx_np, E in cases:
+        idx = torch.from_numpy(idx_np).cuda()
+        got = _offsets_static(moe, idx, E)
+        want = _oracle_tables(oracle, idx_np, E)
+        for g, r in zip(got, want):
+            np.testing.assert_array_equal(g, r, err_msg=name)
+
+
 def test_offsets_static_rejects_sizes_beyond_its_scratch(moe):
     L = moe.lib()
     idx = torch.zeros(1, 1, dtype=torch.int64, device="cuda")
