@@ -38,18 +38,21 @@ sys.path.insert(0, ROOT)
 from moe_expert_layer_counts_gb300 import inputs  # noqa: E402
 
 METRIC = "MoE fwd TFLOP/s & tokens/s (T=8192,H=7168,I=2048,E=256,k=8); % FP8 peak"
-STAGES = ("route", "dispatch", "expert_l1", "expert_l2", "combine")
+STAGES = ("route", "dispatch", "experts", "combine")             # what moe_forward runs (fused expert kernel)
+STAGES_SEPARATE = ("route", "dispatch", "expert_l1", "expert_l2", "combine")
 ROUTE_CHUNK = 2048  # top-k entries the one-kernel plan handles
 FLUSH_BYTES = 512 << 20
 # FLOPs of one oracle sample (about 7 s on 16 host cores at the full layer size)
 ORACLE_SAMPLE_FLOP = 4.0e11
 
 
-def kernels_per_step(w) -> int:
+def kernels_per_step(w, fused=True) -> int:
     """Kernels of the library one step launches: the plan (route_count,
     route_scan, route_slot, or route_small for at most ROUTE_CHUNK top-k
-    entries), dispatch_quant, the two expert GEMMs and combine."""
-    return (1 if w.T * w.k <= ROUTE_CHUNK else 3) + 4
+    entries), dispatch_quant, the expert kernel(s) and combine.  The fused
+    expert kernel is one launch (its readiness counters are zeroed by a
+    memset node, not a kernel of the library)."""
+    return (1 if w.T * w.k <= ROUTE_CHUNK else 3) + (3 if fused else 4)
 
 
 def peaks():
@@ -249,55 +252,62 @@ class Layer:
         # FP4 codes + UE8M0 scales of every touched expert (W1 and W2)
         self.weight_bytes = self.touched * 3 * w.H * w.I * (0.5 + 1.0 / 32)
 
-    def step(self, ev=None):
+    def step(self, ev=None, fused=True):
+        """One step; with fused=False the two expert layers run as two
+        launches (moe_expert_l1, moe_expert_l2) so that each can be timed."""
         m, w, d = self.moe, self.w, self.d
-        if ev: ev[0].record()
+        rec = iter(ev) if ev else None
+        if rec: next(rec).record()
         p = m.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I, workspace=self.ws)
-        if ev: ev[1].record()
+        if rec: next(rec).record()
         m.dispatch(p, d["x"])
-        if ev: ev[2].record()
-        m.expert_l1(p, self.W1)
-        if ev: ev[3].record()
-        m.expert_l2(p, self.W2)
-        if ev: ev[4].record()
+        if rec: next(rec).record()
+        if fused:
+            m.expert_fused(p, self.W1, self.W2)
+        else:
+            m.expert_l1(p, self.W1)
+            if rec: next(rec).record()
+            m.expert_l2(p, self.W2)
+        if rec: next(rec).record()
         m.combine(p, self.y)
-        if ev: ev[5].record()
+        if rec: next(rec).record()
         return p
 
-    def l1_bytes(self):
-        """Algorithmic bytes of one L1 launch: the touched experts' W1 (codes +
-        scales), the pool rows read (codes + scales) and h written."""
+    def expert_bytes(self):
+        """Algorithmic bytes of one fused expert launch: the touched experts' W1
+        and W2 (codes + scales), the pool rows read (codes + scales) and the
+        bf16 L2 rows written (h stays an intermediate of the launch)."""
         w = self.w
-        return (self.touched * 2 * w.I * w.H * (0.5 + 1.0 / 32) + self.n_valid * w.H * (1 + 1.0 / 32)
-                + self.n_valid * w.I * (1 + 1.0 / 32))
+        return self.weight_bytes + self.n_valid * w.H * (1 + 1.0 / 32) + self.n_valid * w.H * 2
 
 
-def timed_steps(L, args, world, flush, dev):
+def timed_steps(L, args, world, flush, dev, fused=True):
     """W untimed steps, then K steps bracketed by barrier + synchronize, each
     after an L2 flush (outside the events); CUDA events per stage."""
     moe = L.moe
+    stages = STAGES if fused else STAGES_SEPARATE
     for _ in range(args.warmup):
         flush.fill_(1)
-        p = L.step()
+        p = L.step(fused=fused)
     torch.cuda.synchronize()
     status = moe.plan_check(p)
     assert status == 0, moe.error_string(status)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         for i in range(args.steps):
             flush.fill_(i & 255)
-            p = L.step(evs[i])
+            p = L.step(evs[i], fused=fused)
         torch.cuda.synchronize()
     barrier(world)
     status = moe.plan_check(p)
     assert status == 0, moe.error_string(status)
-    stage_ms = {s: 0.0 for s in STAGES}
+    stage_ms = {s: 0.0 for s in stages}
     total_ms = 0.0
     for e in evs:
-        total_ms += e[0].elapsed_time(e[5])
-        for j, s in enumerate(STAGES):
+        total_ms += e[0].elapsed_time(e[-1])
+        for j, s in enumerate(stages):
             stage_ms[s] += e[j].elapsed_time(e[j + 1])
     t_max = max_over_ranks(total_ms / 1e3, world)
     return t_max, {s: v / args.steps for s, v in stage_ms.items()}, clk.summary()
@@ -311,29 +321,45 @@ def weight_stream(L, step_s, pk):
 
 
 def roofline(L, stage_ms, pk, mma):
-    """The dominant kernel, L1: tensor-bound against the FP8 peak (and the
-    measured block-scaled MMA ceiling) when experts hold more than 16 rows,
-    otherwise bound by its weight stream from HBM."""
+    """The dominant kernel, the fused expert kernel (both GEMMs): tensor-bound
+    against the FP8 peak (and the measured block-scaled MMA ceiling) when
+    experts hold more than 16 rows, otherwise bound by its weight stream from
+    HBM."""
     w = L.w
-    l1_s = stage_ms["expert_l1"] / 1e3
+    t_s = stage_ms["experts"] / 1e3
+    kernel = "expert_gemm_kernel<3> (L1 + L2 fused)"
     if L.max_count <= 16:
-        gb = L.l1_bytes()
-        ach = gb / l1_s / 1e9
-        return dict(kernel="expert_gemm_kernel<1> (L1)", bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s",
+        gb = L.expert_bytes()
+        ach = gb / t_s / 1e9
+        return dict(kernel=kernel, bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s",
                     frac=ach / pk["hbm_gbs"], traffic=measured_traffic(w.name),
-                    algorithmic=f"touched W1 (codes + scales) + pool rows read + h written = {gb:.4g} B per launch",
+                    algorithmic=f"touched W1 + W2 (codes + scales) + pool rows read + L2 rows written = {gb:.4g} B "
+                                f"per launch",
                     peak_note=f"{pk['source']} HBM copy bandwidth")
-    fl = 4.0 * L.n_valid * w.H * w.I
-    ach = fl / l1_s / 1e12
+    fl = 6.0 * L.n_valid * w.H * w.I
+    ach = fl / t_s / 1e12
     fp8 = 2.0 * pk["bf16"]
-    r = dict(kernel="expert_gemm_kernel<1> (L1)", bound="tensor", achieved=ach, peak=fp8, unit="TFLOP/s",
+    r = dict(kernel=kernel, bound="tensor", achieved=ach, peak=fp8, unit="TFLOP/s",
              frac=ach / fp8, traffic=measured_traffic(w.name),
-             algorithmic=f"4*N*H*I = {fl:.4g} FLOP per launch (valid rows only)",
+             algorithmic=f"6*N*H*I = {fl:.4g} FLOP per launch (valid rows only)",
              peak_note=f"FP8 = 2 x {pk['source']} burst bf16 cuBLAS rate ({pk['bf16']} TF/s), the nominal FP8/bf16 "
                        f"ratio of the dense tensor rates")
     if mma:
         r.update(frac_vs_mma=ach / mma["tflops"], mma_ceiling_tflops=mma["tflops"])
     return r
+
+
+def separate_leg(L, args, world, flush, dev, pk):
+    """The same steps with the two expert layers as two launches: per-layer
+    times and tensor rates (L1 4*N*H*I, L2 2*N*H*I FLOP)."""
+    t, stage_ms, _ = timed_steps(L, args, world, flush, dev, fused=False)
+    w = L.w
+    fp8 = 2.0 * pk["bf16"]
+    out = dict(ms_per_step=1e3 * t / args.steps, stage_ms=stage_ms)
+    for name, f in (("expert_l1", 4.0), ("expert_l2", 2.0)):
+        tf = f * L.n_valid * w.H * w.I / (stage_ms[name] / 1e3) / 1e12
+        out[name] = dict(tflops=tf, frac_fp8=tf / fp8)
+    return out
 
 
 def mma_ceiling(moe):
@@ -354,7 +380,8 @@ def decode_leg(moe, args, world, flush, dev, pk):
     out = dict(workload=f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} k={w.k}", ms_per_step=1e3 * step_s,
                value=world * L.flops / step_s / 1e12, unit="TFLOP/s", tokens_per_s=world * w.T / step_s,
                stage_ms=stage_ms, weight_stream=weight_stream(L, step_s, pk), roofline=roofline(L, stage_ms, pk, None),
-               clocks=clk, gpu_launches=kernels_per_step(w) * args.steps)
+               clocks=clk, gpu_launches=kernels_per_step(w) * args.steps,
+               separate_kernels=separate_leg(L, args, world, flush, dev, pk))
     del L
     torch.cuda.empty_cache()
     return out
@@ -503,6 +530,7 @@ def main():
     t_max, stage_ms, clk = timed_steps(L, args, world, flush, dev)
     value = world * L.flops * args.steps / t_max / 1e12
     step_s = t_max / args.steps
+    separate = separate_leg(L, args, world, flush, dev, pk)
     e2e = e2e_legs(L, args, world, flush)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -523,6 +551,7 @@ def main():
         mma_ceiling=mma,
         stage_ms=stage_ms,
         roofline=roofline(L, stage_ms, pk, mma),
+        separate_kernels=separate,
         e2e=e2e,
         gpu_launches=kernels_per_step(w) * args.steps,
         clocks=clk,

@@ -178,14 +178,34 @@ int moe_expert_l1(const moe_plan_t* plan, const moe_weights_t* W1, const moe_opt
  * combine buffer).  W2: E, N = H, K = I must match the plan. */
 int moe_expert_l2(const moe_plan_t* plan, const moe_weights_t* W2, void* stream);
 
+/* Both expert layers in ONE persistent launch (the single-kernel design of
+ * the pages: DeepEP -> Mega MoE page, the sm100_fp8_fp4_mega_moe.cuh
+ * compute pipeline and its on-chip L1 -> L2 hand-off; Normal-vs-Low-Latency
+ * page sections 6.2-6.3, the scheduler's block phases and the wait of an L2
+ * block on its L1 arrival count).  Computes exactly what moe_expert_l1 +
+ * moe_expert_l2 compute (the same bytes of h and of the L2 rows).  Work items
+ * are all layer-1 tiles (pool row block x 128 intermediate columns), then all
+ * layer-2 tiles (row block x 256 output columns), spread over one CTA per
+ * SM; a layer-2 tile of row block b starts once every layer-1 tile of b has
+ * stored its h rows (a per-block counter in the workspace, zeroed by this
+ * call).  So the last layer-1 wave is filled with layer-2 work and the
+ * second launch disappears.  The wait is bounded: if a block is not ready
+ * within 1 s of global time the launch records MOE_ERR_TIMEOUT (error word 1
+ * = 81, see MOE_EXPORT_ERROR) and its CTAs exit; the wait needs every CTA of
+ * the launch resident at once (one per SM), so it may time out if other work
+ * holds SMs for that long.  W1, W2 and opts as for moe_expert_l1 /
+ * moe_expert_l2. */
+int moe_expert_fused(const moe_plan_t* plan, const moe_weights_t* W1, const moe_weights_t* W2,
+                     const moe_options_t* opts, void* stream);
+
 /* Combine (DeepEP -> Mega MoE page, combine_utils.cuh snippet; Dispatch/
  * Combine page section 5.1): y[t] = bf16(fp32 sum over ascending j of the
  * valid entries' L2 rows), y[t] = 0 if token t has no valid entry.
  * y [T, H] bf16. */
 int moe_combine(const moe_plan_t* plan, void* y, void* stream);
 
-/* The whole layer after moe_plan(): moe_dispatch + moe_expert_l1 +
- * moe_expert_l2 + moe_combine, in stream order; opts may be NULL. */
+/* The whole layer after moe_plan(): moe_dispatch + moe_expert_fused +
+ * moe_combine, in stream order; opts may be NULL. */
 int moe_forward(const void* x, const moe_weights_t* W1, const moe_weights_t* W2,
                 const moe_plan_t* plan, void* y, const moe_options_t* opts, void* stream);
 
@@ -211,7 +231,11 @@ enum {
     MOE_EXPORT_H_Q = 11,         /* uint8 [P_cap, I] E4M3 requantised L1 output */
     MOE_EXPORT_H_SF = 12,        /* uint8 [P_cap/128][I/128][512] UE8M0, tensor-core layout */
     MOE_EXPORT_L2_OUT = 13,      /* bf16 [P_cap, H] L2 output rows in pool order */
-    MOE_EXPORT_ERROR = 14,       /* int32 [2] device error record: bits, then where a wait expired */
+    MOE_EXPORT_ERROR = 14,       /* int32 [2] device error record: bits, then 1 + where a wait expired
+                                  * (0-15 producer on a stage, 16 MMA on the accumulator, 32-47 MMA on a
+                                  * stage, 48 epilogue, 64-79 scale copies, 80 a fused layer-2 tile on
+                                  * its row block's layer-1 tiles, 96 producer on its work-item queue,
+                                  * 97 a warp waiting for its next work item) */
     MOE_EXPORT_POOL_ROWS = 15,   /* (size only) P_cap, the pool row capacity, in the size field */
     MOE_EXPORT_MAX_COUNT = 16    /* int32 [1] largest expert count (0 when nothing is routed) */
 };
@@ -275,6 +299,15 @@ int moe_selftest_bounded_wait(int arrive, uint64_t timeout_ns, int32_t* out, voi
  *   ctas     out (host): the number of CTAs launched (the SM count)
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (not sm_103), MOE_ERR_CUDA. */
 int moe_selftest_mma_rate(int kblocks, int32_t* status, int* ctas, void* stream);
+
+/* Failure-detection self-test of moe_expert_fused (no counterpart on the
+ * pages): runs the fused launch with its readiness counters set so that no
+ * row block ever becomes ready, so every layer-2 tile's bounded wait expires
+ * after 1 s.  The launch then records MOE_ERR_TIMEOUT in the plan's
+ * workspace (read it with moe_plan_check) and exits without a fault or a
+ * trap; the context stays usable.  Layer-1 outputs are written as usual,
+ * layer-2 outputs are invalid.  Arguments as for moe_expert_fused. */
+int moe_selftest_fused_wait(const moe_plan_t* plan, const moe_weights_t* W1, const moe_weights_t* W2, void* stream);
 
 /* Static text for a status code. */
 const char* moe_error_string(int status);

@@ -8,7 +8,7 @@ missing, loading fails loudly; there is no other implementation to fall back
 to.
 
 Names follow the C ABI: ``plan`` (moe_plan), ``dispatch``, ``expert_l1``,
-``expert_l2``, ``combine``, ``forward`` (moe_forward), ``plan_check``.
+``expert_l2``, ``expert_fused``, ``combine``, ``forward`` (moe_forward), ``plan_check``.
 """
 from __future__ import annotations
 
@@ -49,7 +49,7 @@ _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",
            "moe_dispatch", "moe_expert_l1", "moe_expert_l2", "moe_combine", "moe_forward", "moe_plan_check",
            "moe_plan_export", "moe_error_string", "moe_expert_offsets_static", "moe_selftest_bounded_wait",
-           "moe_selftest_mma_rate")
+           "moe_selftest_mma_rate", "moe_expert_fused", "moe_selftest_fused_wait")
 
 
 class MoeError(RuntimeError):
@@ -114,6 +114,12 @@ def lib():
             L.moe_expert_l1.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights), OP, P]
             L.moe_expert_l2.restype = i32
             L.moe_expert_l2.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights), P]
+            L.moe_expert_fused.restype = i32
+            L.moe_expert_fused.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights), ctypes.POINTER(Weights),
+                                           OP, P]
+            L.moe_selftest_fused_wait.restype = i32
+            L.moe_selftest_fused_wait.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(Weights),
+                                                  ctypes.POINTER(Weights), P]
             L.moe_forward.restype = i32
             L.moe_forward.argtypes = [P, ctypes.POINTER(Weights), ctypes.POINTER(Weights), ctypes.POINTER(Plan), P,
                                       OP, P]
@@ -242,6 +248,19 @@ def expert_l1(p: MoePlan, W1: MXFP4Weight, options: Options | None = None, strea
 
 def expert_l2(p: MoePlan, W2: MXFP4Weight, stream=None):
     _check(lib().moe_expert_l2(ctypes.byref(p.c), ctypes.byref(W2.c), _stream(stream)), "moe_expert_l2")
+
+
+def expert_fused(p: MoePlan, W1: MXFP4Weight, W2: MXFP4Weight, options: Options | None = None, stream=None):
+    """moe_expert_fused: both expert layers in one persistent launch."""
+    _check(lib().moe_expert_fused(ctypes.byref(p.c), ctypes.byref(W1.c), ctypes.byref(W2.c), _opts(options),
+                                  _stream(stream)), "moe_expert_fused")
+
+
+def selftest_fused_wait(p: MoePlan, W1: MXFP4Weight, W2: MXFP4Weight, stream=None):
+    """moe_selftest_fused_wait: the fused launch with no row block ever ready
+    (every layer-2 wait expires); read the outcome with plan_check."""
+    _check(lib().moe_selftest_fused_wait(ctypes.byref(p.c), ctypes.byref(W1.c), ctypes.byref(W2.c),
+                                         _stream(stream)), "moe_selftest_fused_wait")
 
 
 def combine(p: MoePlan, y: torch.Tensor, stream=None):

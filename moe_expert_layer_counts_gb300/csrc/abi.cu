@@ -146,6 +146,7 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
     L->h_q = take(static_cast<size_t>(cap) * I);
     L->h_sf = take(static_cast<size_t>(cap / kBlockM) * (I / 128) * kSfChunkBytes);
     L->l2_out = take(static_cast<size_t>(cap) * H * 2);
+    L->sched = take(sizeof(int) * (kSchedWords + static_cast<size_t>(cap / kBlockM)));
     L->total = o;
     return true;
 }
@@ -254,6 +255,32 @@ int moe_expert_l2(const moe_plan_t* plan, const moe_weights_t* W2, void* stream)
     return expert_layer(2, plan, W2, nullptr, stream);
 }
 
+static int expert_fused(const moe_plan_t* plan, const moe_weights_t* W1, const moe_weights_t* W2,
+                        const moe_options_t* opts, void* stream, bool publish) {
+    const PlanState* ps = plan_state(plan);
+    moe_options_t o;
+    if (!ps || !read_options(opts, &o)) return MOE_ERR_INVALID_ARG;
+    int rc = check_weights(W1, ps->E, 2 * ps->I, ps->H);
+    if (rc) return rc;
+    if ((rc = check_weights(W2, ps->E, ps->H, ps->I))) return rc;
+    int sms = 0;
+    if ((rc = device_info(&sms))) return rc;
+    Layout L;
+    if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
+    GemmLaunch g1{W1->q, W1->sf_mma, W1->E, W1->N, W1->K, o.activation_clamp, o.scale_rule, o.fast_math};
+    GemmLaunch g2{W2->q, W2->sf_mma, W2->E, W2->N, W2->K, 0.0f, MOE_SCALE_CEIL, 1};
+    return cuda_status(launch_expert_fused(L, ps->ws, g1, g2, sms, static_cast<cudaStream_t>(stream), publish));
+}
+
+int moe_expert_fused(const moe_plan_t* plan, const moe_weights_t* W1, const moe_weights_t* W2,
+                     const moe_options_t* opts, void* stream) {
+    return expert_fused(plan, W1, W2, opts, stream, true);
+}
+
+int moe_selftest_fused_wait(const moe_plan_t* plan, const moe_weights_t* W1, const moe_weights_t* W2, void* stream) {
+    return expert_fused(plan, W1, W2, nullptr, stream, false);
+}
+
 int moe_combine(const moe_plan_t* plan, void* y, void* stream) {
     const PlanState* ps = plan_state(plan);
     if (!ps || (ps->T > 0 && !y) || (reinterpret_cast<uintptr_t>(y) & 15u)) return MOE_ERR_INVALID_ARG;
@@ -270,8 +297,7 @@ int moe_forward(const void* x, const moe_weights_t* W1, const moe_weights_t* W2,
     moe_options_t o;
     if (!read_options(opts, &o)) return MOE_ERR_INVALID_ARG;
     if ((rc = moe_dispatch(plan, x, &o, stream))) return rc;
-    if ((rc = moe_expert_l1(plan, W1, &o, stream))) return rc;
-    if ((rc = moe_expert_l2(plan, W2, stream))) return rc;
+    if ((rc = moe_expert_fused(plan, W1, W2, &o, stream))) return rc;
     return moe_combine(plan, y, stream);
 }
 

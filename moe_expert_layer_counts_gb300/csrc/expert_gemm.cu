@@ -97,7 +97,13 @@ static_assert(kRingOff + kNarrowStages * kNarrowStride <= kSmemEnd, "narrow ring
 constexpr int kSmemBytes = kSmemEnd + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kSfTmemCol + 16 * kMaxStages <= kTmemCols, "scale slots");
-constexpr uint64_t kWaitNs = 1000000000ull;    // 1 s per wait
+// Bounded waits: 1 s for the producer thread, whose waits are the only ones
+// that depend on anything outside the CTA (its copies, the work counter and,
+// fused, other CTAs' layer-1 tiles); 2 s for every wait downstream of it, so
+// that when something outside stalls, the producer's wait expires first and
+// the error record names the root cause.
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint64_t kReaderWaitNs = 2 * kWaitNs;
 
 struct GemmParams {
     const int* n_blocks;
@@ -120,7 +126,16 @@ struct GemmParams {
     int fast_math;          // layer 1: 0 = every SwiGLU value by the exact formula
     const int* block_rows;  // valid rows of each pool row block (plan)
     const int* max_count;   // largest expert count (plan): selects the ring shape
+    const uint8_t* a_rows;  // A operand rows (pool or h), K bytes each
 };
+
+// Work items are handed out by a global counter (dynamic scheduling: a CTA
+// takes its next item when it starts the current one).  The producer thread
+// takes them and passes each item number to the MMA thread, the scale warp
+// and the epilogue warps through a small queue in shared memory; a number at
+// or beyond the item count ends the CTA's loop.
+constexpr int kQueue = 4;
+constexpr int kItemReaders = 2 + kEpiWarps;   // MMA thread, scale warp, epilogue warps
 
 struct Shared {
     uint64_t full[kMaxStages];
@@ -130,6 +145,9 @@ struct Shared {
     uint64_t tmem_full;
     uint64_t tmem_empty;
     uint64_t drain;
+    uint64_t item_full[kQueue];
+    uint64_t item_empty[kQueue];
+    int item[kQueue];
     uint32_t tmem_base;
     int abort;
 };
@@ -137,16 +155,40 @@ struct Shared {
 // On expiry the first CTA to give up records where: err[1] = 1 + where, with
 // where = stage (producer waiting on empty), 16 (MMA on tmem_empty),
 // 32 + stage (MMA on the stage's operands and scales), 48 (epilogue on
-// tmem_full), 64 + stage (scale warp on the stage's operands).
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, Shared* sh, int* err, int where) {
+// tmem_full), 64 + stage (scale warp on the stage's operands), 80 (fused: a
+// layer-2 tile on its row block's layer-1 tiles), 96 (producer on a queue
+// slot), 97 (a reader on the next item number).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, Shared* sh, int* err, int where,
+                                              uint64_t wait_ns = kReaderWaitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (ptx::mbar_wait(bar, parity, ptx::globaltimer() + kWaitNs)) return true;
+    if (ptx::mbar_wait(bar, parity, ptx::globaltimer() + wait_ns)) return true;
     atomicOr(err, kDevErrTimeout);
     atomicCAS(err + 1, 0, 1 + where);
     *reinterpret_cast<volatile int*>(&sh->abort) = 1;
     return false;
 }
 __device__ __forceinline__ bool aborted(Shared* sh) { return *reinterpret_cast<volatile int*>(&sh->abort) != 0; }
+
+// Producer side of the item queue: the seq-th item number of this CTA into
+// slot seq % kQueue, once every reader has taken the item kQueue before it.
+__device__ __forceinline__ bool put_item(Shared* sh, int seq, int w, int* err) {
+    const int slot = seq & (kQueue - 1);
+    if (seq >= kQueue &&
+        !wait_or_abort(ptx::smem_addr(&sh->item_empty[slot]), ((seq / kQueue) - 1) & 1, sh, err, 96, kWaitNs))
+        return false;
+    sh->item[slot] = w;
+    ptx::mbar_arrive(ptx::smem_addr(&sh->item_full[slot]));  // release: the number is visible to the readers
+    return true;
+}
+// Reader side: the seq-th item number (one thread per reader); -1 if the
+// wait expired.
+__device__ __forceinline__ int get_item(Shared* sh, int seq, int* err) {
+    const int slot = seq & (kQueue - 1);
+    if (!wait_or_abort(ptx::smem_addr(&sh->item_full[slot]), (seq / kQueue) & 1, sh, err, 97)) return -1;
+    const int w = sh->item[slot];
+    ptx::mbar_arrive(ptx::smem_addr(&sh->item_empty[slot]));
+    return w;
+}
 
 // SwiGLU of one value by the exact definition, (float)(g / (1 + exp(-g))) in
 // double; kept out of line so the rare callers stay small.
@@ -352,22 +394,77 @@ __device__ __forceinline__ void store_out_rows(const CUtensorMap* map, uint8_t* 
     }
 }
 
-template <int kLayer, bool kClamp>
-__global__ void __launch_bounds__(kThreads, 1)
-    expert_gemm_kernel(const __grid_constant__ Maps maps, const __grid_constant__ CUtensorMap tmap_b,
-                       const GemmParams p) {
+// Everything a launch needs, for both layers: the tensor maps (grid constants,
+// which the TMA unit reads in parameter space) and each layer's parameters.
+// A one-layer launch uses entry layer-1; the fused launch uses both.
+struct KernelArgs {
+    Maps maps[2];            // A boxes of each layer (+ layer 2's output map)
+    CUtensorMap tmap_b[2];   // W1 as a 3-D map (expert-half, row, K), W2 as a 2-D map
+    GemmParams p[2];
+    int* l1_done;            // fused: per pool row block, epilogue warps done with its h rows
+    int* work_ctr;           // items handed out beyond the first gridDim.x (zero at launch)
+};
+
+// Work item w -> (layer, pool row block, tile).  kMode 1 or 2: that layer's
+// items, block-major.  kMode 3 (fused): all of layer 1's items first, then
+// all of layer 2's, so an item only ever waits on items before it.
+template <int kMode>
+__device__ __forceinline__ void decode_item(const KernelArgs& ka, int w, int n_work1, int& layer, int& b, int& j) {
+    if (kMode == 3) {
+        layer = w < n_work1 ? 1 : 2;
+        if (layer == 2) w -= n_work1;
+    } else {
+        layer = kMode;
+    }
+    const int nt = ka.p[layer - 1].n_tiles;
+    b = w / nt;
+    j = w % nt;
+}
+
+// Fused launch: the layer-2 items of row block b wait until every epilogue
+// warp of every layer-1 tile of b has stored its h rows and scales (release
+// on the writer side: each lane fences, then one lane counts the warp in).
+// Bounded: past the deadline the error is recorded and the CTA aborts.  The
+// proxy fence orders the acquired generic-proxy view of h before the TMA
+// (async-proxy) loads that follow.
+__device__ __forceinline__ bool wait_l1_block(const int* counter, int target, Shared* sh, int* err) {
+    if (ptx::ld_acquire_gpu(counter) < target) {
+        const uint64_t deadline = ptx::globaltimer() + kWaitNs;
+        while (ptx::ld_acquire_gpu(counter) < target) {
+            if (aborted(sh)) return false;
+            if (ptx::globaltimer() > deadline) {
+                atomicOr(err, kDevErrTimeout);
+                atomicCAS(err + 1, 0, 1 + 80);
+                *reinterpret_cast<volatile int*>(&sh->abort) = 1;
+                return false;
+            }
+            __nanosleep(128);
+        }
+    }
+    ptx::fence_proxy_async_global();
+    return true;
+}
+
+// kMode 1 / 2: one layer; kMode 3: both layers in one persistent launch.
+template <int kMode, bool kClamp>
+__global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_constant__ KernelArgs ka) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Shared* sh = reinterpret_cast<Shared*>(smem);
     uint8_t* ring = smem + kRingOff;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // fields both layers share (the plan's tables, the error record)
+    const GemmParams& p0 = ka.p[kMode == 2 ? 1 : 0];
 
-    const int n_work = *p.n_blocks * p.n_tiles;
+    const int n_blocks = *p0.n_blocks;
+    const int n_work1 = kMode == 2 ? 0 : n_blocks * ka.p[0].n_tiles;
+    const int n_work = kMode == 1 ? n_work1
+                       : kMode == 2 ? n_blocks * ka.p[1].n_tiles
+                                    : n_work1 + n_blocks * ka.p[1].n_tiles;
     if (static_cast<int>(blockIdx.x) >= n_work) return;  // uniform for the CTA
-    const int kb_count = p.K / kBlockK;
     // ring shape (uniform for the launch)
-    const bool narrow = *p.max_count <= kNarrowRows;
+    const bool narrow = *p0.max_count <= kNarrowRows;
     const int n_stages = narrow ? kNarrowStages : kWideStages;
     const int stride = narrow ? kNarrowStride : kWideStride;
     const int a_bytes = narrow ? kNarrowABytes : kWideABytes;
@@ -383,11 +480,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(ptx::smem_addr(&sh->tmem_full), 1);
         ptx::mbar_init(ptx::smem_addr(&sh->tmem_empty), kEpiWarps);
         ptx::mbar_init(ptx::smem_addr(&sh->drain), 1);
+        for (int q = 0; q < kQueue; ++q) {
+            ptx::mbar_init(ptx::smem_addr(&sh->item_full[q]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh->item_empty[q]), kItemReaders);
+        }
         sh->abort = 0;
         ptx::fence_mbar_init();
-        for (int i = 0; i < kABoxLevels; ++i) ptx::prefetch_tensormap(&maps.box[i]);
-        ptx::prefetch_tensormap(&tmap_b);
-        if (kLayer == 2) ptx::prefetch_tensormap(&maps.out);
+        for (int l = (kMode == 2 ? 1 : 0); l < (kMode == 1 ? 1 : 2); ++l) {
+            for (int i = 0; i < kABoxLevels; ++i) ptx::prefetch_tensormap(&ka.maps[l].box[i]);
+            ptx::prefetch_tensormap(&ka.tmap_b[l]);
+        }
+        if (kMode != 1) ptx::prefetch_tensormap(&ka.maps[1].out);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&sh->tmem_base), kTmemCols);
@@ -403,41 +506,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
-        bool ok = true;
-        const int pairs = (p.N + 255) / 256;
-        // the block metadata of the next work item is loaded one item ahead, so
-        // its latency never stalls the stream of copies at a tile boundary
-        int next_b = blockIdx.x / p.n_tiles;
-        int next_e = __ldg(p.block_expert + next_b);
-        int next_rows = __ldg(p.block_rows + next_b);
-        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-            const int b = next_b, j = w % p.n_tiles, e = next_e, rows = next_rows;
-            if (w + static_cast<int>(gridDim.x) < n_work) {
-                next_b = (w + static_cast<int>(gridDim.x)) / p.n_tiles;
-                next_e = __ldg(p.block_expert + next_b);
-                next_rows = __ldg(p.block_rows + next_b);
+        bool ok;
+        // Item numbers: the first is blockIdx.x, every later one comes from the
+        // work counter when the previous one starts, so the block metadata of
+        // the next item is loaded one item ahead and its latency never stalls
+        // the stream of copies at a tile boundary.
+        int seq = 0;
+        int w = blockIdx.x;
+        int layer, b, j;
+        decode_item<kMode>(ka, w, n_work1, layer, b, j);
+        int e = __ldg(p0.block_expert + b), rows = __ldg(p0.block_rows + b);
+        ok = put_item(sh, seq++, w, p0.err);
+        while (ok) {
+            const int wn = min(n_work, static_cast<int>(gridDim.x) + atomicAdd(ka.work_ctr, 1));
+            if (!put_item(sh, seq++, wn, p0.err)) {
+                ok = false;
+                break;
+            }
+            int next_layer = 0, next_b = 0, next_j = 0, next_e = 0, next_rows = 0;
+            if (wn < n_work) {
+                decode_item<kMode>(ka, wn, n_work1, next_layer, next_b, next_j);
+                next_e = __ldg(p0.block_expert + next_b);
+                next_rows = __ldg(p0.block_rows + next_b);
+            }
+            const GemmParams& P = ka.p[layer - 1];
+            const int kb_count = P.K / kBlockK;
+            const int pairs = (P.N + 255) / 256;
+            if (kMode == 3 && layer == 2 && !wait_l1_block(ka.l1_done + b, kEpiWarps * ka.p[0].n_tiles, sh, p0.err)) {
+                ok = false;
+                break;
             }
             // layer 1: gate|up halves of expert e, rows j*128 of each (3-D map: K, row, expert-half)
             // layer 2: rows e*H + 256*j .. +256 (2-D map)
-            const int b_y = kLayer == 1 ? j * 128 : e * p.N + j * kBN;
-            const int b_z = kLayer == 1 ? 2 * e : 0;
-            const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
-            const uint8_t* sfb = p.sfb + (static_cast<size_t>(e) * pairs + j) * kb_count * 2 * kSfChunkBytes;
+            const int b_y = layer == 1 ? j * 128 : e * P.N + j * kBN;
+            const int b_z = layer == 1 ? 2 * e : 0;
+            const uint8_t* sfa = P.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
+            const uint8_t* sfb = P.sfb + (static_cast<size_t>(e) * pairs + j) * kb_count * 2 * kSfChunkBytes;
             const int level = a_box_level(rows);  // the A box that covers the block's valid rows
             const uint32_t tx = kStageTxBytes - (kBlockM - (16 << level)) * kBlockK;
+            const CUtensorMap* map_a = &ka.maps[layer - 1].box[level];
+            const CUtensorMap* map_b = &ka.tmap_b[layer - 1];
             for (int kb = 0; kb < kb_count; ++kb) {
-                if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p.err, stage)) {
+                if (aborted(sh) ||
+                    !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p0.err, stage, kWaitNs)) {
                     ok = false;
                     break;
                 }
                 uint8_t* st = ring + stage * stride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
                 ptx::mbar_arrive_expect_tx(full, tx);
-                ptx::tma_load_2d(ptx::smem_addr(st), &maps.box[level], kb * kBlockK, b * kBlockM, full);
-                if (kLayer == 1)
-                    ptx::tma_load_3d(ptx::smem_addr(st + a_bytes), &tmap_b, kb * kBlockK, b_y, b_z, full);
+                ptx::tma_load_2d(ptx::smem_addr(st), map_a, kb * kBlockK, b * kBlockM, full);
+                if (layer == 1)
+                    ptx::tma_load_3d(ptx::smem_addr(st + a_bytes), map_b, kb * kBlockK, b_y, b_z, full);
                 else
-                    ptx::tma_load_2d(ptx::smem_addr(st + a_bytes), &tmap_b, kb * kBlockK, b_y, full);
+                    ptx::tma_load_2d(ptx::smem_addr(st + a_bytes), map_b, kb * kBlockK, b_y, full);
                 ptx::bulk_load(ptx::smem_addr(st + sf_off), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
                 ptx::bulk_load(ptx::smem_addr(st + sf_off + kSfChunkBytes), sfb + kb * 2 * kSfChunkBytes,
                                2 * kSfChunkBytes, full);
@@ -448,6 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     phase ^= 1;
                 }
             }
+            if (wn >= n_work) break;
+            w = wn;
+            layer = next_layer;
+            b = next_b;
+            j = next_j;
+            e = next_e;
+            rows = next_rows;
         }
         if (!ok) {
             // let this CTA's copies in flight land before the CTA may exit
@@ -475,12 +604,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
-            if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->tmem_empty), acc_phase ^ 1, sh, p.err, 16)) break;
+        for (int seq = 0; ok; ++seq) {
+            const int w = get_item(sh, seq, p0.err);
+            if (w < 0 || w >= n_work) break;
+            const int kb_count = ka.p[(kMode == 3 ? (w < n_work1 ? 1 : 2) : kMode) - 1].K / kBlockK;
+            if (aborted(sh) || !wait_or_abort(ptx::smem_addr(&sh->tmem_empty), acc_phase ^ 1, sh, p0.err, 16)) break;
             ptx::tc_fence_after();
             for (int kb = 0; kb < kb_count; ++kb) {
                 // the stage's operands have landed and its scales are in tensor memory
-                if (!wait_or_abort(ready0 + 8 * stage, phase, sh, p.err, 32 + stage)) {
+                if (!wait_or_abort(ready0 + 8 * stage, phase, sh, p0.err, 32 + stage)) {
                     ok = false;
                     break;
                 }
@@ -520,9 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+        for (int seq = 0; ok; ++seq) {
+            const int w = get_item(sh, seq, p0.err);
+            if (w < 0 || w >= n_work) break;
+            const int kb_count = ka.p[(kMode == 3 ? (w < n_work1 ? 1 : 2) : kMode) - 1].K / kBlockK;
             for (int kb = 0; kb < kb_count; ++kb) {
-                if (!wait_or_abort(full0 + 8 * stage, phase, sh, p.err, 64 + stage)) {
+                if (!wait_or_abort(full0 + 8 * stage, phase, sh, p0.err, 64 + stage)) {
                     ok = false;
                     break;
                 }
@@ -552,36 +687,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = quad * 32 + lane;                 // row of the tile = tensor-memory lane
         const uint32_t t_row = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         uint32_t acc_phase = 0;
-        for (int w = blockIdx.x; w < n_work; w += gridDim.x) {
-            const int b = w / p.n_tiles, j = w % p.n_tiles;
+        for (int seq = 0;; ++seq) {
+            int w = 0;
+            if (lane == 0) w = get_item(sh, seq, p0.err);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (w < 0 || w >= n_work) break;
+            int layer, b, j;
+            decode_item<kMode>(ka, w, n_work1, layer, b, j);
             const int r = b * kBlockM + m;
-            const int tok = __ldg(p.row_token + r);
-            const float wgt = __ldg(p.row_weight + r);
+            const int tok = __ldg(p0.row_token + r);
+            const float wgt = __ldg(p0.row_weight + r);
             // tcgen05.ld is warp-collective: the whole warp goes on or stops together
-            const bool go = !aborted(sh) && wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p.err, 48);
+            const bool go = !aborted(sh) && wait_or_abort(ptx::smem_addr(&sh->tmem_full), acc_phase, sh, p0.err, 48);
             if (!__all_sync(0xffffffffu, go)) break;
             ptx::tc_fence_after();
             uint32_t pk[64];
-            drain_accumulator<kLayer>(t_row, half, pk, [&] {
-                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
-            });
-            if (kLayer == 1) {
-                if (tok >= 0) store_h_row<kClamp>(p, b, j, r, quad, half, lane, wgt, pk);
+            if (kMode != 2 && layer == 1) {
+                drain_accumulator<1>(t_row, half, pk, [&] {
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
+                });
+                if (tok >= 0) store_h_row<kClamp>(ka.p[0], b, j, r, quad, half, lane, wgt, pk);
+                if (kMode == 3) {
+                    // this warp's h codes and scale bytes are stored: count it in for block b
+                    ptx::fence_proxy_async_global();
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(ka.l1_done + b, 1);
+                }
             } else {
+                drain_accumulator<2>(t_row, half, pk, [&] {
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh->tmem_empty));
+                });
+                const GemmParams& P = ka.p[1];
                 const int col0 = j * kBN + 128 * half;  // H is a multiple of 128: a half is all in or all out
                 const uint32_t routed = __ballot_sync(0xffffffffu, tok >= 0);
-                if (col0 < p.H) {
+                if (col0 < P.H) {
                     if (!narrow && routed == 0xffffffffu)
-                        store_out_rows(&maps.out, smem + kOutStageOff + (warp - 2) * kOutStageBytes, col0,
+                        store_out_rows(&ka.maps[1].out, smem + kOutStageOff + (warp - 2) * kOutStageBytes, col0,
                                        b * kBlockM + quad * 32, lane, pk);
                     else if (tok >= 0)
-                        store_out_rows_direct(p, r, col0, pk);
+                        store_out_rows_direct(P, r, col0, pk);
                 }
             }
             acc_phase ^= 1;
         }
         // this warp's tensor stores complete before the CTA exits
-        if (kLayer == 2 && lane == 0) ptx::bulk_wait_all();
+        if (kMode != 1 && lane == 0) ptx::bulk_wait_all();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -590,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_dealloc(tmem, kTmemCols);
     }
 #else
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, kDevErrTimeout);
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(ka.p[0].err, kDevErrTimeout);
 #endif
 }
 
@@ -662,7 +813,7 @@ namespace {
 // Opt a kernel into its dynamic shared memory once per device.
 template <typename Kernel>
 cudaError_t smem_attr_once(Kernel kernel, int slot, int bytes) {
-    static int done[3][64] = {};
+    static int done[5][64] = {};
     int dev = 0;
     cudaError_t st = cudaGetDevice(&dev);
     if (st != cudaSuccess) return st;
@@ -676,47 +827,10 @@ cudaError_t smem_attr_once(Kernel kernel, int slot, int bytes) {
 
 namespace {
 
-// One CTA per SM, 128-row tiles: B arrives as one request per stage (a 3-D
-// map brings the gate and up rows for layer 1, a 256-row box for layer 2).
-cudaError_t launch_gemm(int layer, const Layout& L, const GemmLaunch& g, const void* a_base, const GemmParams& p,
-                          int num_sms, cudaStream_t s) {
-    CUtensorMap map_b;
-    Maps maps;
-    bool maps_ok = true;
-    for (int i = 0; i < kABoxLevels; ++i)
-        maps_ok = maps_ok && make_map(&maps.box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, a_base, g.K, L.p_cap, g.K, 16u << i);
-    if (layer == 2)
-        maps_ok = maps_ok && make_out_map(&maps.out, p.out_bf16, L.H, L.p_cap);
-    else
-        maps.out = maps.box[0];  // unused by layer 1
-    if (layer == 1)  // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
-        maps_ok = maps_ok && make_map_3d_fp4(&map_b, g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
-    else
-        maps_ok = maps_ok && make_map(&map_b, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K,
-                                      static_cast<uint64_t>(g.E) * g.N, g.K / 2, kBN);
-    if (!maps_ok) return cudaErrorInvalidValue;
-    cudaError_t st;
-    if (layer == 1) {
-        if (p.clamp != std::numeric_limits<float>::infinity()) {
-            if ((st = smem_attr_once(expert_gemm_kernel<1, true>, 2, kSmemBytes)) != cudaSuccess) return st;
-            expert_gemm_kernel<1, true><<<num_sms, kThreads, kSmemBytes, s>>>(maps, map_b, p);
-        } else {
-            if ((st = smem_attr_once(expert_gemm_kernel<1, false>, 0, kSmemBytes)) != cudaSuccess) return st;
-            expert_gemm_kernel<1, false><<<num_sms, kThreads, kSmemBytes, s>>>(maps, map_b, p);
-        }
-    } else {
-        if ((st = smem_attr_once(expert_gemm_kernel<2, false>, 1, kSmemBytes)) != cudaSuccess) return st;
-        expert_gemm_kernel<2, false><<<num_sms, kThreads, kSmemBytes, s>>>(maps, map_b, p);
-    }
-    return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,
-                               cudaStream_t s) {
-    if (L.T == 0) return cudaSuccess;
-    GemmParams p{};
+// The maps and parameters of one layer (index layer-1 of the launch's args).
+bool fill_layer(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, KernelArgs* ka) {
+    GemmParams& p = ka->p[layer - 1];
+    p = GemmParams{};
     p.n_blocks = reinterpret_cast<const int*>(ws + L.n_blocks);
     p.block_expert = reinterpret_cast<const int*>(ws + L.block_expert);
     p.row_token = reinterpret_cast<const int*>(ws + L.row_token);
@@ -732,20 +846,70 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     p.clamp = g.clamp > 0.0f ? g.clamp : std::numeric_limits<float>::infinity();  // no clamp
     p.scale_rule = g.scale_rule;
     p.fast_math = g.fast_math;
-    const void* a_base;
+    Maps& maps = ka->maps[layer - 1];
+    bool ok = true;
     if (layer == 1) {
-        a_base = ws + L.pool_q;
+        p.a_rows = ws + L.pool_q;
         p.sfa = ws + L.pool_sf;
         p.out_q = ws + L.h_q;
         p.out_sf = ws + L.h_sf;
         p.n_tiles = L.I / 128;
+        maps.out = CUtensorMap{};  // unused by layer 1
+        // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
+        ok = make_map_3d_fp4(&ka->tmap_b[0], g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
     } else {
-        a_base = ws + L.h_q;
+        p.a_rows = ws + L.h_q;
         p.sfa = ws + L.h_sf;
         p.out_bf16 = reinterpret_cast<uint16_t*>(ws + L.l2_out);
         p.n_tiles = (L.H + kBN - 1) / kBN;
+        ok = make_out_map(&maps.out, p.out_bf16, L.H, L.p_cap) &&
+             make_map(&ka->tmap_b[1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w_q, g.K,
+                      static_cast<uint64_t>(g.E) * g.N, g.K / 2, kBN);
     }
-    return launch_gemm(layer, L, g, a_base, p, num_sms, s);
+    for (int i = 0; i < kABoxLevels; ++i)
+        ok = ok && make_map(&maps.box[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, p.a_rows, g.K, L.p_cap, g.K, 16u << i);
+    return ok;
+}
+
+template <int kMode, bool kClamp>
+cudaError_t launch_mode(const KernelArgs& ka, int slot, int num_sms, cudaStream_t s) {
+    cudaError_t st = smem_attr_once(expert_gemm_kernel<kMode, kClamp>, slot, kSmemBytes);
+    if (st != cudaSuccess) return st;
+    if (kMode != 3 && (st = cudaMemsetAsync(ka.work_ctr, 0, sizeof(int), s)) != cudaSuccess) return st;
+    expert_gemm_kernel<kMode, kClamp><<<num_sms, kThreads, kSmemBytes, s>>>(ka);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,
+                               cudaStream_t s) {
+    if (L.T == 0) return cudaSuccess;
+    KernelArgs ka{};
+    if (!fill_layer(layer, L, ws, g, &ka)) return cudaErrorInvalidValue;
+    ka.work_ctr = reinterpret_cast<int*>(ws + L.sched) + (layer - 1);
+    const bool clamp = ka.p[layer - 1].clamp != std::numeric_limits<float>::infinity();
+    if (layer == 1) return clamp ? launch_mode<1, true>(ka, 2, num_sms, s) : launch_mode<1, false>(ka, 0, num_sms, s);
+    return launch_mode<2, false>(ka, 1, num_sms, s);
+}
+
+cudaError_t launch_expert_fused(const Layout& L, uint8_t* ws, const GemmLaunch& g1, const GemmLaunch& g2, int num_sms,
+                                cudaStream_t s, bool publish) {
+    if (L.T == 0) return cudaSuccess;
+    KernelArgs ka{};
+    if (!fill_layer(1, L, ws, g1, &ka) || !fill_layer(2, L, ws, g2, &ka)) return cudaErrorInvalidValue;
+    // The work counter and the readiness counters start at zero for every
+    // launch.  (Self-test only: with publish == false the readiness counters
+    // start at 0x80808080, a large negative count that the layer-1 tiles can
+    // never raise to the target, so every layer-2 tile's bounded wait runs out.)
+    ka.work_ctr = reinterpret_cast<int*>(ws + L.sched) + 2;
+    ka.l1_done = reinterpret_cast<int*>(ws + L.sched) + kSchedWords;
+    const size_t blocks = static_cast<size_t>(L.p_cap / kBlockM);
+    cudaError_t st = cudaMemsetAsync(ws + L.sched, 0, sizeof(int) * (kSchedWords + blocks), s);
+    if (st != cudaSuccess) return st;
+    if (!publish && (st = cudaMemsetAsync(ka.l1_done, 0x80, sizeof(int) * blocks, s)) != cudaSuccess) return st;
+    const bool clamp = ka.p[0].clamp != std::numeric_limits<float>::infinity();
+    return clamp ? launch_mode<3, true>(ka, 4, num_sms, s) : launch_mode<3, false>(ka, 3, num_sms, s);
 }
 
 }  // namespace moe

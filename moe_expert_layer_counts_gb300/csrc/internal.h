@@ -16,6 +16,7 @@ constexpr int kSfChunkBytes = 512;     // 128 rows x 4 scales, tensor-core layou
 constexpr int kRouteChunk = 2048;      // top-k entries per routing CTA
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopk = 32;
+constexpr int kSchedWords = 4;         // work counters at the head of the scheduler region
 
 // Device-side error bits recorded in the workspace (word 0); word 1 records
 // where a bounded wait expired.
@@ -30,6 +31,8 @@ struct Layout {
     size_t err, n_blocks, max_count, count, off, poff, hist, chunk_base, block_expert, block_rows;
     size_t slot_of, row_token, row_topk, row_weight;
     size_t pool_q, pool_sf, h_q, h_sf, l2_out;
+    size_t sched;      // expert kernels: work counters (L1, L2, fused), then per row block the
+                       // layer-1 epilogue warps done (fused kernel's readiness counters)
     size_t total;
 };
 
@@ -67,5 +70,11 @@ struct GemmLaunch {
 // layer 1: pool x W1 -> requantised h; layer 2: h x W2 -> bf16 rows.
 cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,
                                cudaStream_t s);
+// Both layers in one persistent launch (layer-2 tiles of a row block start once
+// that block's layer-1 tiles have stored h).
+// publish == false is the failure-detection self-test: no row block ever
+// becomes ready, so every layer-2 tile's bounded wait expires.
+cudaError_t launch_expert_fused(const Layout& L, uint8_t* ws, const GemmLaunch& g1, const GemmLaunch& g2, int num_sms,
+                                cudaStream_t s, bool publish = true);
 
 }  // namespace moe

@@ -80,6 +80,8 @@ def lib():
             L.or_forward.restype = i32
             L.or_forward.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P, P, i32, P, P, P, P, P, i64,
                                      ctypes.c_float, i32, i32]
+            L.or_l2_combine.restype = i32
+            L.or_l2_combine.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, i64, P, i32, P, i32]
             L.or_combine.restype = None
             L.or_combine.argtypes = [P, P, i32, i32, i32, P]
             L.or_bruteforce_token.restype = i32
@@ -242,6 +244,27 @@ def forward(x_bf16_bits, topk_idx, topk_w, E, w1q, w1sf, w2q, w2sf, tokens=None,
     if hq is not None:
         res.update(hq=hq, hsf=hsf, o=o, h=hf)
     return res
+
+
+def l2_combine(topk_idx, topk_w, E, w2q, w2sf, hq_pool, hsf_pool, tokens, nthreads: int = 0):
+    """L2 + combine of the listed tokens from given requantised L1 outputs
+    (hq_pool uint8 [p_cap, I], hsf_pool uint8 [p_cap, I/32], indexed by the
+    plan's pool rows): the second half of forward(), to replay the layer
+    from another implementation's h.  Returns y (uint16 bf16 bits [ntok, H])."""
+    idx = _c(topk_idx, np.int64)
+    T, k = idx.shape
+    w = _c(topk_w, np.float32)
+    w2q, w2sf = _c(w2q, np.uint8), _c(w2sf, np.uint8)
+    H, I = w2q.shape[1], w2q.shape[2] * 2
+    hq, hsf = _c(hq_pool, np.uint8), _c(hsf_pool, np.uint8)
+    p_cap = hq.shape[0]
+    assert hq.shape == (p_cap, I) and hsf.shape == (p_cap, I // SF_VEC) and p_cap >= pool_capacity(T, k, E)
+    toks = _c(tokens, np.int32)
+    y = np.zeros((toks.size, H), np.uint16)
+    st = lib().or_l2_combine(_p(idx), _p(w), T, k, E, H, I, _p(w2q), _p(w2sf), _p(hq), _p(hsf), p_cap, _p(toks),
+                             toks.size, _p(y), nthreads)
+    assert st in (0, 1), st
+    return y
 
 
 def combine(o_pool: np.ndarray, slot_of: np.ndarray, T: int, k: int):

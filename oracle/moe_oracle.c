@@ -266,17 +266,15 @@ static float clamp_act(float v, float c) {
     return v;
 }
 
-/* One (token, expert) row of the FFN.
+/* L1 of one (token, expert) row: gate/up accumulators (double sum -> fp32
+ * -> bf16), SwiGLU * top-k weight in fp32, requantised to MXFP8 along I.
  *   xq/xsf : the token's E4M3 codes [H] and UE8M0 bytes [H/32]
  *   w1d    : dequantised W1 of the expert [2I, H]   (gate rows 0..I-1, up I..2I-1)
- *   w2d    : dequantised W2 of the expert [H, I]
  *   weight : the top-k weight of this (token, j) entry
- * Outputs: hq[I] / hsf[I/32] (requantised SwiGLU*w), o[H] (bf16 bits). */
-static void ffn_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, const float* w2d,
-                    int H, int I, float weight, float clamp, int rule, double* xd, double* hd, float* h,
-                    uint8_t* hq, uint8_t* hsf, uint16_t* o) {
+ * Outputs: h[I] (fp32 SwiGLU*w), hq[I] / hsf[I/32] (its MXFP8 form). */
+static void l1_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, int H, int I, float weight,
+                   float clamp, int rule, double* xd, float* h, uint8_t* hq, uint8_t* hsf) {
     for (int c = 0; c < H; ++c) xd[c] = or_e4m3_decode(xq[c]) * or_ue8m0_value(xsf[c / OR_SF_VEC]);
-    /* L1: gate and up accumulators, double sum -> fp32 -> bf16 */
     for (int n = 0; n < I; ++n) {
         double ag = 0.0, au = 0.0;
         const float* wg = w1d + (size_t)n * H;
@@ -289,16 +287,27 @@ static void ffn_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, con
         float hu = silu * u;
         h[n] = hu * weight;
     }
-    /* requantise to MXFP8 along I */
     or_quant_mx_e4m3_rule(h, I, hq, hsf, rule);
+}
+
+/* L2 of one row: o[c] = bf16(double sum over i of deq(hq)*deq(W2[c])), unweighted.
+ *   w2d : dequantised W2 of the expert [H, I] */
+static void l2_row(const uint8_t* hq, const uint8_t* hsf, const float* w2d, int H, int I, double* hd, uint16_t* o) {
     for (int i = 0; i < I; ++i) hd[i] = or_e4m3_decode(hq[i]) * or_ue8m0_value(hsf[i / OR_SF_VEC]);
-    /* L2: double sum -> fp32 -> bf16, unweighted */
     for (int c = 0; c < H; ++c) {
         double acc = 0.0;
         const float* w = w2d + (size_t)c * I;
         for (int i = 0; i < I; ++i) acc += hd[i] * (double)w[i];
         o[c] = or_bf16_encode((float)acc);
     }
+}
+
+/* One (token, expert) row of the FFN: l1_row then l2_row. */
+static void ffn_row(const uint8_t* xq, const uint8_t* xsf, const float* w1d, const float* w2d,
+                    int H, int I, float weight, float clamp, int rule, double* xd, double* hd, float* h,
+                    uint8_t* hq, uint8_t* hsf, uint16_t* o) {
+    l1_row(xq, xsf, w1d, H, I, weight, clamp, rule, xd, h, hq, hsf);
+    l2_row(hq, hsf, w2d, H, I, hd, o);
 }
 
 /* Token-major MXFP8 quantisation of x (bf16 bits [T,H]). */
@@ -420,6 +429,69 @@ int or_forward(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
         }
     }
     free(want); free(xq); free(xsf); free(o_ent); free(w1d); free(w2d); free(rows);
+done:
+    free(count); free(off); free(poff); free(slot_of); free(row_token); free(row_topk); free(row_weight);
+    return st;
+}
+
+/* L2 and combine of the listed tokens from GIVEN requantised L1 outputs
+ * hq_pool [p_cap, I] / hsf_pool [p_cap, I/32] (row-major, indexed by the
+ * plan's pool rows): the second half of or_forward (the same l2_row and the
+ * same combine), used to replay the layer from another implementation's h.
+ * y [ntok, H] in list order.  Returns the or_plan status. */
+int or_l2_combine(const int64_t* topk_idx, const float* topk_w, int T, int k, int E, int H, int I,
+                  const uint8_t* w2q, const uint8_t* w2sf, const uint8_t* hq_pool, const uint8_t* hsf_pool,
+                  int64_t p_cap, const int32_t* tokens, int ntok, uint16_t* y, int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    int64_t n = (int64_t)T * k;
+    int32_t* count = (int32_t*)malloc(sizeof(int32_t) * (E + 1));
+    int32_t* off = (int32_t*)malloc(sizeof(int32_t) * (E + 1));
+    int32_t* poff = (int32_t*)malloc(sizeof(int32_t) * (E + 1));
+    int32_t* slot_of = (int32_t*)malloc(sizeof(int32_t) * (n > 0 ? n : 1));
+    int32_t* row_token = (int32_t*)malloc(sizeof(int32_t) * (p_cap > 0 ? p_cap : 1));
+    int32_t* row_topk = (int32_t*)malloc(sizeof(int32_t) * (p_cap > 0 ? p_cap : 1));
+    float* row_weight = (float*)malloc(sizeof(float) * (p_cap > 0 ? p_cap : 1));
+    int st = or_plan(topk_idx, topk_w, T, k, E, p_cap, count, off, poff, slot_of, row_token, row_topk, row_weight);
+    if (st > 1) goto done;
+    int32_t* want = (int32_t*)malloc(sizeof(int32_t) * (T > 0 ? T : 1));
+    for (int t = 0; t < T; ++t) want[t] = -1;
+    for (int i = 0; i < ntok; ++i) want[tokens[i]] = i;
+    uint16_t* o_ent = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)ntok * k * H + 2);
+    float* w2d = (float*)malloc(sizeof(float) * (size_t)H * I + 4);
+    int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * (p_cap > 0 ? p_cap : 1));
+    for (int e = 0; e < E; ++e) {
+        int nr = 0;
+        for (int32_t r = poff[e]; r < poff[e] + count[e]; ++r)
+            if (want[row_token[r]] >= 0) rows[nr++] = r;
+        if (nr == 0) continue;
+        dequant_expert(w2q, w2sf, e, H, I, w2d);
+#pragma omp parallel
+        {
+            double* hd = (double*)malloc(sizeof(double) * (size_t)I);
+            uint16_t* o = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+            for (int ir = 0; ir < nr; ++ir) {
+                int32_t r = rows[ir];
+                l2_row(hq_pool + (size_t)r * I, hsf_pool + (size_t)r * (I / OR_SF_VEC), w2d, H, I, hd, o);
+                memcpy(o_ent + ((size_t)want[row_token[r]] * k + row_topk[r]) * H, o, sizeof(uint16_t) * H);
+            }
+            free(hd); free(o);
+        }
+    }
+    for (int i = 0; i < ntok; ++i) {
+        int t = tokens[i];
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                if (slot_of[(size_t)t * k + j] < 0) continue;
+                acc = acc + or_bf16_decode(o_ent[((size_t)i * k + j) * H + c]);
+            }
+            y[(size_t)i * H + c] = or_bf16_encode(acc);
+        }
+    }
+    free(want); free(o_ent); free(w2d); free(rows);
 done:
     free(count); free(off); free(poff); free(slot_of); free(row_token); free(row_topk); free(row_weight);
     return st;

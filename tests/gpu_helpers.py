@@ -1,6 +1,19 @@
 """Shared helpers of the GPU parity tests: build inputs on the device, run the
 oracle on the same bytes, convert tensor-core scale layouts back to
-row-major, and the output tolerance of the layer."""
+row-major, and the output tolerance of the layer.
+
+The output bar (relative L2 <= 5e-3 and max-abs <= 2e-2 * rms(y_oracle)) is
+checked element by element against the oracle.  One source of difference is
+inherent: the GPU accumulates gate/up in fp32 on the tensor cores, the
+oracle in double, so where the exact sum lies within fp32 accumulation error
+of a bf16 rounding midpoint the two round gate (or up) to neighbouring bf16
+values, and that one h value can requantise to a neighbouring E4M3 code (a
+few per ten million values).  Such a flip moves the token's y by about one
+bf16 ulp, which exceeds the max-abs bar where |y| > 2.56 * rms(y).  Where the
+bar fails, check_forward therefore requires (1) every element over the bar to
+belong to a token whose pool rows hold such an h flip, (2) flips in at most
+1e-5 of the h values, and (3) the GPU's y to meet the bar against the
+oracle's own L2 + combine replayed from the GPU's h codes and scales."""
 from __future__ import annotations
 
 import numpy as np
@@ -81,3 +94,40 @@ def assert_close_output(y_gpu_bits: np.ndarray, y_ref_bits: np.ndarray, what: st
     if nrm == 0:
         assert np.all(a == 0), f"{what}: oracle output is zero, GPU output is not"
     return rel, mx / max(rms, 1e-30)
+
+
+def check_forward(oracle, p, y, h, E, tokens=None, what="y", activation_clamp=0.0, scale_rule=0):
+    """The GPU forward's y (all tokens, or the listed ones) against the oracle
+    on the same inputs and options, with the rule for inherent gate/up bf16
+    flips described in the module docstring.  Returns the oracle result."""
+    ref = oracle.forward(h["x"], h["topk_idx"], h["topk_w"], E, h["w1q"], h["w1sf"], h["w2q"], h["w2sf"],
+                         tokens=tokens, want_pool=True, activation_clamp=activation_clamp, scale_rule=scale_rule)
+    yg = bits(y) if tokens is None else bits(y)[tokens]
+    try:
+        assert_close_output(yg, ref["y"], what)
+        return ref
+    except AssertionError as first:
+        failure = str(first)
+    T, k = h["topk_idx"].shape
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    a, b = bf16_values(yg), bf16_values(ref["y"])
+    rms = np.sqrt(np.mean(b * b))
+    rel = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+    assert rel <= REL_L2, failure
+    over = np.unique(np.nonzero(np.abs(a - b) > MAX_ABS_RMS * rms)[0])
+    I = h["w2q"].shape[2] * 2
+    cap = p.export("pool_rows")
+    slots = p.export("slot_of").cpu().numpy().reshape(T, k)[toks]
+    rows = slots[slots >= 0]
+    hq_all = p.export("h_q").cpu().numpy().reshape(-1, I)
+    hsf_all = sf_rows_from_mma(p.export("h_sf").cpu().numpy(), cap, I)
+    flip = (hq_all[rows] != ref["hq"][rows]).any(1) | (hsf_all[rows] != ref["hsf"][rows]).any(1)
+    n_flip = int((hq_all[rows] != ref["hq"][rows]).sum() + (hsf_all[rows] != ref["hsf"][rows]).sum())
+    assert n_flip <= 1e-5 * rows.size * I, f"{failure}; and {n_flip} h values differ"
+    flipped_rows = set(rows[flip].tolist())
+    for t in over:
+        assert any(int(s) in flipped_rows for s in slots[t] if s >= 0), \
+            f"{failure}; token {toks[t]} is over the bar without an h flip upstream"
+    y2 = oracle.l2_combine(h["topk_idx"], h["topk_w"], E, h["w2q"], h["w2sf"], hq_all, hsf_all, toks)
+    assert_close_output(yg, y2, what + " (against the oracle's L2 + combine of the GPU's h)")
+    return ref

@@ -22,8 +22,7 @@ def test_forward_all_tokens(moe, oracle, name):
     d, W1, W2 = gh.setup(moe, w)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], name)
+    gh.check_forward(oracle, p, y, gh.host(d), w.E, what=name)
 
 
 @pytest.mark.parametrize("name", ["share", "full", "decode"])
@@ -38,9 +37,17 @@ def test_forward_sampled_tokens_full_size(moe, oracle, name):
     if name == "share":  # include tokens with no local expert (y must be 0)
         none = np.nonzero((h["topk_idx"] < 0).all(1))[0][:3]
         toks = np.unique(np.concatenate([toks, none])).astype(np.int32)
-    ref = gh.oracle_forward(oracle, h, w.E, tokens=toks)
+    ref = gh.check_forward(oracle, p, y, h, w.E, tokens=toks, what=name)
     yb = gh.bits(y)[toks]
-    gh.assert_close_output(yb, ref["y"], name)
+    # the requantised L1 output of the sampled tokens' pool rows, code by code
+    # (wide ring, 128-row A boxes and the full-size layer-1 epilogue here;
+    # the narrow ring on decode): the same bar as on the small workloads
+    slots = p.export("slot_of").cpu().numpy().reshape(w.T, w.k)[toks]
+    rows = slots[slots >= 0]
+    hq = p.export("h_q").cpu().numpy().reshape(-1, w.I)[rows]
+    hsf = gh.sf_rows_from_mma(p.export("h_sf").cpu().numpy(), p.export("pool_rows"), w.I)[rows]
+    assert rows.size > 0
+    assert np.mean(hq != ref["hq"][rows]) <= 1e-5 and np.mean(hsf != ref["hsf"][rows]) <= 1e-5
     if name == "share":
         for t in np.nonzero((h["topk_idx"][toks] < 0).all(1))[0]:
             assert np.all(yb[t] == 0)
@@ -73,8 +80,7 @@ def test_forward_edge_routings(moe, oracle):
         d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
         p, y = run(moe, w, d, W1, W2)
         assert moe.plan_check(p) == 0
-        ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-        gh.assert_close_output(gh.bits(y), ref["y"], name)
+        gh.check_forward(oracle, p, y, gh.host(d), w.E, what=name)
         if name == "none":
             assert torch.all(y.view(torch.int16) == 0)
 
@@ -88,8 +94,7 @@ def test_bad_expert_ids_reported(moe, oracle):
     d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == moe.ERR_BAD_EXPERT_ID
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], "bad ids")
+    gh.check_forward(oracle, p, y, gh.host(d), w.E, what="bad ids")
 
 
 def test_empty_batch_forward(moe):
@@ -109,8 +114,7 @@ def test_odd_h_tail_tile(moe, oracle):
     d, W1, W2 = gh.setup(moe, w)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], "oddH")
+    gh.check_forward(oracle, p, y, gh.host(d), w.E, what="oddH")
 
 
 def test_largest_expert_count_and_topk(moe, oracle):
@@ -121,8 +125,7 @@ def test_largest_expert_count_and_topk(moe, oracle):
     d, W1, W2 = gh.setup(moe, w)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], "E=1024 k=32")
+    gh.check_forward(oracle, p, y, gh.host(d), w.E, what="E=1024 k=32")
 
 
 def test_partial_blocks_on_every_a_box_size(moe, oracle):
@@ -137,8 +140,7 @@ def test_partial_blocks_on_every_a_box_size(moe, oracle):
     d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
-    gh.assert_close_output(gh.bits(y), ref["y"], "partial blocks")
+    gh.check_forward(oracle, p, y, gh.host(d), w.E, what="partial blocks")
 
 
 @pytest.mark.parametrize("largest,H", [(16, 1024), (17, 1024), (16, 384)])
@@ -159,6 +161,5 @@ def test_ring_shape_switch(moe, oracle, largest, H):
     d, W1, W2 = gh.setup(moe, w, idx=idx, tw=tw)
     p, y = run(moe, w, d, W1, W2)
     assert moe.plan_check(p) == 0
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)
     assert int(p.export("max_count").cpu()[0]) == largest
-    gh.assert_close_output(gh.bits(y), ref["y"], f"ring, largest count {largest}, H {H}")
+    gh.check_forward(oracle, p, y, gh.host(d), w.E, what=f"ring, largest count {largest}, H {H}")

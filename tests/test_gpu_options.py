@@ -41,9 +41,8 @@ def test_forward_with_options_against_oracle(moe, oracle, name, clamp, rule):
     p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I)
     y = moe.forward(d["x"], W1, W2, p, options=opts)
     assert moe.plan_check(p) == 0
-    ref = oracle.forward(h["x"], h["topk_idx"], h["topk_w"], w.E, h["w1q"], h["w1sf"], h["w2q"], h["w2sf"],
-                         want_pool=True, activation_clamp=clamp, scale_rule=rule)
-    gh.assert_close_output(gh.bits(y), ref["y"], f"y {name} clamp={clamp} rule={rule}")
+    ref = gh.check_forward(oracle, p, y, h, w.E, what=f"y {name} clamp={clamp} rule={rule}",
+                           activation_clamp=clamp, scale_rule=rule)
     # the requantised L1 output: codes and scales as the oracle's (up to rare bf16 gate/up differences)
     cap = p.export("pool_rows")
     row_token = p.export("row_token").cpu().numpy()

@@ -25,8 +25,7 @@ def test_bounded_wait_times_out_and_context_stays_usable(moe, oracle):
     p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I)
     y = moe.forward(d["x"], W1, W2, p)
     assert moe.plan_check(p) == 0
-    ref = gh.oracle_forward(oracle, gh.host(d), w.E)["y"]
-    gh.assert_close_output(gh.bits(y), ref)
+    gh.check_forward(oracle, p, y, gh.host(d), w.E)
 
 
 def test_bounded_wait_argument_checks(moe):

@@ -229,3 +229,30 @@ def test_tokens_without_valid_entry_are_zero(oracle):
     y = oracle.forward(_bits(d["x"]), idx, d["topk_w"].numpy(), E, *args)["y"]
     assert np.all(y[3] == 0)
     assert np.any(y[5] != 0)
+
+
+def test_l2_combine_replay_matches_forward(oracle):
+    """or_l2_combine, fed the oracle's own requantised h, reproduces the
+    forward's y bit for bit (all tokens and a subset, with skipped entries);
+    one changed h code changes only the y row of the token it belongs to."""
+    T, H, I, E, k = 24, 128, 64, 4, 3
+    w, d = _small(T, H, I, E, k, seed=11)
+    x = _bits(d["x"])
+    idx = d["topk_idx"].numpy().copy()
+    idx[2, 1] = -1
+    idx[5] = -1
+    tw = d["topk_w"].numpy()
+    args = [d[n].numpy() for n in ("w1q", "w1sf", "w2q", "w2sf")]
+    full = oracle.forward(x, idx, tw, E, *args, want_pool=True)
+    all_t = np.arange(T, dtype=np.int32)
+    y = oracle.l2_combine(idx, tw, E, args[2], args[3], full["hq"], full["hsf"], all_t)
+    np.testing.assert_array_equal(y, full["y"])
+    sub = np.array([7, 5, 0], np.int32)
+    np.testing.assert_array_equal(oracle.l2_combine(idx, tw, E, args[2], args[3], full["hq"], full["hsf"], sub),
+                                  full["y"][sub])
+    hq = full["hq"].copy()
+    r = oracle.plan(idx, tw, E)["slot_of"].reshape(T, k)[9, 0]
+    hq[r, 3] ^= 0x08                      # one code one step away
+    y3 = oracle.l2_combine(idx, tw, E, args[2], args[3], hq, full["hsf"], all_t)
+    changed = np.nonzero((y3 != full["y"]).any(1))[0]
+    assert changed.tolist() == [9]
