@@ -148,9 +148,9 @@ def kernel_source_hash() -> str:
 
 
 def measured_traffic(workload: str):
-    """Per-launch DRAM bytes of the L1 kernel on this workload from the
+    """Per-launch DRAM bytes of the fused expert kernel on this workload from the
     committed ncu summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "expert_l1_traffic.json")
+    path = os.path.join(ROOT, "profiles", "expert_traffic.json")
     if not os.path.exists(path):
         return None
     m = json.load(open(path))

@@ -402,6 +402,7 @@ struct KernelArgs {
     CUtensorMap tmap_b[2];   // W1 as a 3-D map (expert-half, row, K), W2 as a 2-D map
     GemmParams p[2];
     int* l1_done;            // fused: per pool row block, epilogue warps done with its h rows
+    int* blocks_done;        // fused: row blocks whose layer-1 tiles are all done
     int* work_ctr;           // items handed out beyond the first gridDim.x (zero at launch)
 };
 
@@ -424,6 +425,9 @@ __device__ __forceinline__ void decode_item(const KernelArgs& ka, int w, int n_w
 // Fused launch: the layer-2 items of row block b wait until every epilogue
 // warp of every layer-1 tile of b has stored its h rows and scales (release
 // on the writer side: each lane fences, then one lane counts the warp in).
+// The warp that completes a block also counts the block in `blocks_done`;
+// once the producer has seen every block counted (one acquire), it skips the
+// per-block check for the rest of the launch.
 // Bounded: past the deadline the error is recorded and the CTA aborts.  The
 // proxy fence orders the acquired generic-proxy view of h before the TMA
 // (async-proxy) loads that follow.
@@ -516,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
         int layer, b, j;
         decode_item<kMode>(ka, w, n_work1, layer, b, j);
         int e = __ldg(p0.block_expert + b), rows = __ldg(p0.block_rows + b);
+        bool all_l1_done = false;  // fused: every row block's layer-1 tiles seen complete
         ok = put_item(sh, seq++, w, p0.err);
         while (ok) {
             const int wn = min(n_work, static_cast<int>(gridDim.x) + atomicAdd(ka.work_ctr, 1));
@@ -532,9 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
             const GemmParams& P = ka.p[layer - 1];
             const int kb_count = P.K / kBlockK;
             const int pairs = (P.N + 255) / 256;
-            if (kMode == 3 && layer == 2 && !wait_l1_block(ka.l1_done + b, kEpiWarps * ka.p[0].n_tiles, sh, p0.err)) {
-                ok = false;
-                break;
+            if (kMode == 3 && layer == 2 && !all_l1_done) {
+                if (ptx::ld_acquire_gpu(ka.blocks_done) >= n_blocks) {
+                    all_l1_done = true;
+                    ptx::fence_proxy_async_global();
+                } else if (!wait_l1_block(ka.l1_done + b, kEpiWarps * ka.p[0].n_tiles, sh, p0.err)) {
+                    ok = false;
+                    break;
+                }
             }
             // layer 1: gate|up halves of expert e, rows j*128 of each (3-D map: K, row, expert-half)
             // layer 2: rows e*H + 256*j .. +256 (2-D map)
@@ -709,10 +719,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
                 if (tok >= 0) store_h_row<kClamp>(ka.p[0], b, j, r, quad, half, lane, wgt, pk);
                 if (kMode == 3) {
                     // this warp's h codes and scale bytes are stored: count it in for block b
+                    // (and the block in blocks_done when this warp completes it)
                     ptx::fence_proxy_async_global();
                     __threadfence();
                     __syncwarp();
-                    if (lane == 0) atomicAdd(ka.l1_done + b, 1);
+                    if (lane == 0 &&
+                        ptx::atom_add_acq_rel_gpu(ka.l1_done + b, 1) == kEpiWarps * ka.p[0].n_tiles - 1)
+                        ptx::atom_add_acq_rel_gpu(ka.blocks_done, 1);  // acq_rel: a chain through every block
                 }
             } else {
                 drain_accumulator<2>(t_row, half, pk, [&] {
@@ -903,6 +916,7 @@ cudaError_t launch_expert_fused(const Layout& L, uint8_t* ws, const GemmLaunch& 
     // start at 0x80808080, a large negative count that the layer-1 tiles can
     // never raise to the target, so every layer-2 tile's bounded wait runs out.)
     ka.work_ctr = reinterpret_cast<int*>(ws + L.sched) + 2;
+    ka.blocks_done = reinterpret_cast<int*>(ws + L.sched) + 3;
     ka.l1_done = reinterpret_cast<int*>(ws + L.sched) + kSchedWords;
     const size_t blocks = static_cast<size_t>(L.p_cap / kBlockM);
     cudaError_t st = cudaMemsetAsync(ws + L.sched, 0, sizeof(int) * (kSchedWords + blocks), s);

@@ -102,14 +102,16 @@ def quantize_mxfp4(w: torch.Tensor):
     e = q - 2 otherwise; both comparisons are exact."""
     N, K = w.shape
     assert K % SF_VEC == 0
-    b = w.to(torch.float64).reshape(N, K // SF_VEC, SF_VEC)
+    # float32 throughout: amax, frexp, the power-of-two scaling and the
+    # comparisons with the (exactly representable) midpoints are all exact
+    b = w.to(torch.float32).reshape(N, K // SF_VEC, SF_VEC)
     amax = b.abs().amax(dim=-1)
     f, q = torch.frexp(amax)
     e = torch.where(f <= 0.75, q - 3, q - 2)
     e = torch.where(amax > 0, e, torch.zeros_like(e)).clamp(-126, 127)
-    v = b * torch.exp2(-e.to(torch.float64))[..., None]
+    v = b * torch.ldexp(torch.ones_like(amax), -e)[..., None]
     a = v.abs()
-    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float64, device=w.device)
+    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float32, device=w.device)
     code = torch.bucketize(a, mids, right=False)          # midpoints strictly below a
     tie = (code < len(_E2M1_MIDS)) & (a == mids[code.clamp(max=len(_E2M1_MIDS) - 1)])
     code = code + (tie & (code % 2 == 1)).to(code.dtype)   # a tie goes to the even code
