@@ -252,7 +252,7 @@ class Layer:
         # FP4 codes + UE8M0 scales of every touched expert (W1 and W2)
         self.weight_bytes = self.touched * 3 * w.H * w.I * (0.5 + 1.0 / 32)
 
-    def step(self, ev=None, fused=True):
+    def step(self, ev=None, fused=True, options=None):
         """One step; with fused=False the two expert layers run as two
         launches (moe_expert_l1, moe_expert_l2) so that each can be timed."""
         m, w, d = self.moe, self.w, self.d
@@ -260,12 +260,12 @@ class Layer:
         if rec: next(rec).record()
         p = m.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I, workspace=self.ws)
         if rec: next(rec).record()
-        m.dispatch(p, d["x"])
+        m.dispatch(p, d["x"], options=options)
         if rec: next(rec).record()
         if fused:
-            m.expert_fused(p, self.W1, self.W2)
+            m.expert_fused(p, self.W1, self.W2, options=options)
         else:
-            m.expert_l1(p, self.W1)
+            m.expert_l1(p, self.W1, options=options)
             if rec: next(rec).record()
             m.expert_l2(p, self.W2)
         if rec: next(rec).record()
@@ -281,14 +281,14 @@ class Layer:
         return self.weight_bytes + self.n_valid * w.H * (1 + 1.0 / 32) + self.n_valid * w.H * 2
 
 
-def timed_steps(L, args, world, flush, dev, fused=True):
+def timed_steps(L, args, world, flush, dev, fused=True, options=None):
     """W untimed steps, then K steps bracketed by barrier + synchronize, each
     after an L2 flush (outside the events); CUDA events per stage."""
     moe = L.moe
     stages = STAGES if fused else STAGES_SEPARATE
     for _ in range(args.warmup):
         flush.fill_(1)
-        p = L.step(fused=fused)
+        p = L.step(fused=fused, options=options)
     torch.cuda.synchronize()
     status = moe.plan_check(p)
     assert status == 0, moe.error_string(status)
@@ -298,7 +298,7 @@ def timed_steps(L, args, world, flush, dev, fused=True):
     with ClockSampler(dev.index) as clk:
         for i in range(args.steps):
             flush.fill_(i & 255)
-            p = L.step(evs[i], fused=fused)
+            p = L.step(evs[i], fused=fused, options=options)
         torch.cuda.synchronize()
     barrier(world)
     status = moe.plan_check(p)
@@ -360,6 +360,17 @@ def separate_leg(L, args, world, flush, dev, pk):
         tf = f * L.n_valid * w.H * w.I / (stage_ms[name] / 1e3) / 1e12
         out[name] = dict(tflops=tf, frac_fp8=tf / fp8)
     return out
+
+
+def gather_leg(L, args, world, flush, dev):
+    """The same steps with layer 1 gathering its A rows by token from
+    token-major x (moe_options_t.a_operand = MOE_A_GATHER: dispatch writes each
+    token's codes once instead of k pool rows; same results)."""
+    t, stage_ms, _ = timed_steps(L, args, world, flush, dev, options=L.moe.Options(a_operand=L.moe.A_GATHER))
+    return dict(ms_per_step=1e3 * t / args.steps, value=world * L.flops * args.steps / t / 1e12, unit="TFLOP/s",
+                stage_ms=stage_ms,
+                note="A operand of layer 1 gathered by token with TMA tile::gather4 (32 four-row requests per "
+                     "128-row stage) instead of one 128-row box of the expert-major pool")
 
 
 def mma_ceiling(moe):
@@ -531,6 +542,7 @@ def main():
     value = world * L.flops * args.steps / t_max / 1e12
     step_s = t_max / args.steps
     separate = separate_leg(L, args, world, flush, dev, pk)
+    gathered = gather_leg(L, args, world, flush, dev)
     e2e = e2e_legs(L, args, world, flush)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -552,6 +564,7 @@ def main():
         stage_ms=stage_ms,
         roofline=roofline(L, stage_ms, pk, mma),
         separate_kernels=separate,
+        a_gather=gathered,
         e2e=e2e,
         gpu_launches=kernels_per_step(w) * args.steps,
         clocks=clk,

@@ -134,7 +134,7 @@ int moe_plan(moe_plan_t* plan, const int64_t* topk_idx, const float* topk_w, int
 
 /* Layer options (the activation_clamp and fast_math arguments of the API on
  * the Normal-vs-Low-Latency page; the pages define neither, so the readings
- * are stated here).  Pass NULL for the defaults {0, MOE_SCALE_CEIL, 1}.
+ * are stated here).  Pass NULL for the defaults {0, MOE_SCALE_CEIL, 1, MOE_A_POOL}.
  *   activation_clamp  > 0: the bf16-rounded gate and up values are limited to
  *                     [-c, c] before SwiGLU; 0 or +inf: no clamp (NaN and
  *                     negative values are MOE_ERR_INVALID_ARG)
@@ -151,11 +151,30 @@ enum {
     MOE_SCALE_CEIL = 0,
     MOE_SCALE_OCP_FLOOR = 1
 };
+/* Where layer 1 takes its FP8 operand rows from (moe_options_t.a_operand):
+ *   MOE_A_POOL    moe_dispatch writes every valid entry's row into the
+ *                 expert-major pool (k copies of a token); layer 1 loads
+ *                 128-row boxes of the pool
+ *   MOE_A_GATHER  moe_dispatch writes each token's MXFP8 row once,
+ *                 token-major, and the pool's scales only; layer 1 gathers
+ *                 the rows of each pool row block by token index with TMA
+ *                 tile::gather4 loads (the "skip the pool" collapse of the
+ *                 Dispatch/Combine page, section 7.2).  Same results, bit
+ *                 for bit; fewer bytes written by dispatch, more TMA requests
+ *                 per layer-1 stage.
+ * moe_dispatch and the layer-1 call (moe_expert_l1 / moe_expert_fused) of one
+ * forward must be given the same a_operand; moe_forward passes one options
+ * value to both. */
+enum {
+    MOE_A_POOL = 0,
+    MOE_A_GATHER = 1
+};
 typedef struct moe_options_t {
     float activation_clamp;
     int32_t scale_rule;
     int32_t fast_math;
-    int32_t reserved[5]; /* must be zero */
+    int32_t a_operand;   /* MOE_A_POOL (default) or MOE_A_GATHER */
+    int32_t reserved[4]; /* must be zero */
 } moe_options_t;
 
 /* Dispatch gather (Dispatch/Combine page section 3.1, token pull into the
@@ -237,7 +256,8 @@ enum {
                                   * its row block's layer-1 tiles, 96 producer on its work-item queue,
                                   * 97 a warp waiting for its next work item) */
     MOE_EXPORT_POOL_ROWS = 15,   /* (size only) P_cap, the pool row capacity, in the size field */
-    MOE_EXPORT_MAX_COUNT = 16    /* int32 [1] largest expert count (0 when nothing is routed) */
+    MOE_EXPORT_MAX_COUNT = 16,   /* int32 [1] largest expert count (0 when nothing is routed) */
+    MOE_EXPORT_X_Q = 17          /* uint8 [T, H] token-major E4M3 x (written by dispatch with MOE_A_GATHER) */
 };
 int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* bytes);
 

@@ -38,12 +38,12 @@ SF_PAIRS_HALVES = 1
 
 EXPORT = dict(count=0, off=1, poff=2, slot_of=3, row_token=4, row_topk=5, row_weight=6, block_expert=7,
               n_blocks=8, pool_q=9, pool_sf=10, h_q=11, h_sf=12, l2_out=13, error=14, pool_rows=15,
-              max_count=16)
+              max_count=16, x_q=17)
 _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_of=torch.int32,
                      row_token=torch.int32, row_topk=torch.int32, row_weight=torch.float32,
                      block_expert=torch.int32, n_blocks=torch.int32, pool_q=torch.uint8, pool_sf=torch.uint8,
                      h_q=torch.uint8, h_sf=torch.uint8, l2_out=torch.bfloat16, error=torch.int32,
-                     max_count=torch.int32)
+                     max_count=torch.int32, x_q=torch.uint8)
 
 # every function declared in include/moe.h
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",
@@ -73,15 +73,22 @@ SCALE_CEIL = 0
 SCALE_OCP_FLOOR = 1
 
 
+A_POOL = 0
+A_GATHER = 1
+
+
 class Options(ctypes.Structure):
     """moe_options_t: activation_clamp (> 0 limits bf16 gate/up to [-c, c]; 0 = off),
     scale_rule (SCALE_CEIL / SCALE_OCP_FLOOR for the activation scales), fast_math
-    (1: fast SwiGLU with exact decisions, 0: exact everywhere; same bytes)."""
+    (1: fast SwiGLU with exact decisions, 0: exact everywhere; same bytes), a_operand
+    (A_POOL: layer 1 reads the expert-major pool; A_GATHER: dispatch writes x once
+    token-major and layer 1 gathers rows by token; same bytes)."""
     _fields_ = [("activation_clamp", ctypes.c_float), ("scale_rule", ctypes.c_int32),
-                ("fast_math", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("fast_math", ctypes.c_int32), ("a_operand", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
-    def __init__(self, activation_clamp: float = 0.0, scale_rule: int = SCALE_CEIL, fast_math: int = 1):
-        super().__init__(float(activation_clamp), int(scale_rule), int(fast_math))
+    def __init__(self, activation_clamp: float = 0.0, scale_rule: int = SCALE_CEIL, fast_math: int = 1,
+                 a_operand: int = A_POOL):
+        super().__init__(float(activation_clamp), int(scale_rule), int(fast_math), int(a_operand))
 
 
 def _opts(options: "Options | None"):

@@ -92,11 +92,12 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA
 
 // Options with defaults filled in; false if a field is out of range.
 bool read_options(const moe_options_t* opts, moe_options_t* o) {
-    *o = moe_options_t{0.0f, MOE_SCALE_CEIL, 1, {0, 0, 0, 0, 0}};
+    *o = moe_options_t{0.0f, MOE_SCALE_CEIL, 1, MOE_A_POOL, {0, 0, 0, 0}};
     if (!opts) return true;
     if (std::isnan(opts->activation_clamp) || opts->activation_clamp < 0.0f) return false;
     if (opts->scale_rule != MOE_SCALE_CEIL && opts->scale_rule != MOE_SCALE_OCP_FLOOR) return false;
     if (opts->fast_math != 0 && opts->fast_math != 1) return false;
+    if (opts->a_operand != MOE_A_POOL && opts->a_operand != MOE_A_GATHER) return false;
     for (int r : opts->reserved)
         if (r != 0) return false;
     *o = *opts;
@@ -146,6 +147,7 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
     L->h_q = take(static_cast<size_t>(cap) * I);
     L->h_sf = take(static_cast<size_t>(cap / kBlockM) * (I / 128) * kSfChunkBytes);
     L->l2_out = take(static_cast<size_t>(cap) * H * 2);
+    L->x_q = take(static_cast<size_t>(std::max(T, 1)) * H);  // token-major MXFP8 x (MOE_A_GATHER)
     L->sched = take(sizeof(int) * (kSchedWords + static_cast<size_t>(cap / kBlockM)));
     L->total = o;
     return true;
@@ -227,7 +229,8 @@ int moe_dispatch(const moe_plan_t* plan, const void* x, const moe_options_t* opt
     if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
     int rc = device_info(nullptr);
     if (rc) return rc;
-    return cuda_status(launch_dispatch(L, ps->ws, x, o.scale_rule, static_cast<cudaStream_t>(stream)));
+    return cuda_status(
+        launch_dispatch(L, ps->ws, x, o.scale_rule, o.a_operand == MOE_A_GATHER, static_cast<cudaStream_t>(stream)));
 }
 
 static int expert_layer(int layer, const moe_plan_t* plan, const moe_weights_t* W, const moe_options_t* opts,
@@ -243,7 +246,8 @@ static int expert_layer(int layer, const moe_plan_t* plan, const moe_weights_t* 
     if ((rc = device_info(&sms))) return rc;
     Layout L;
     if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
-    GemmLaunch g{W->q, W->sf_mma, W->E, W->N, W->K, o.activation_clamp, o.scale_rule, o.fast_math};
+    GemmLaunch g{W->q, W->sf_mma, W->E, W->N, W->K, o.activation_clamp, o.scale_rule, o.fast_math,
+                 layer == 1 && o.a_operand == MOE_A_GATHER};
     return cuda_status(launch_expert_gemm(layer, L, ps->ws, g, sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -267,8 +271,9 @@ static int expert_fused(const moe_plan_t* plan, const moe_weights_t* W1, const m
     if ((rc = device_info(&sms))) return rc;
     Layout L;
     if (!make_layout(ps->T, ps->k, ps->E, ps->H, ps->I, &L)) return MOE_ERR_INVALID_ARG;  // a valid plan always has one
-    GemmLaunch g1{W1->q, W1->sf_mma, W1->E, W1->N, W1->K, o.activation_clamp, o.scale_rule, o.fast_math};
-    GemmLaunch g2{W2->q, W2->sf_mma, W2->E, W2->N, W2->K, 0.0f, MOE_SCALE_CEIL, 1};
+    GemmLaunch g1{W1->q, W1->sf_mma, W1->E, W1->N, W1->K, o.activation_clamp, o.scale_rule, o.fast_math,
+                  o.a_operand == MOE_A_GATHER};
+    GemmLaunch g2{W2->q, W2->sf_mma, W2->E, W2->N, W2->K, 0.0f, MOE_SCALE_CEIL, 1, false};
     return cuda_status(launch_expert_fused(L, ps->ws, g1, g2, sms, static_cast<cudaStream_t>(stream), publish));
 }
 
@@ -339,6 +344,7 @@ int moe_plan_export(const moe_plan_t* plan, int what, size_t* offset, size_t* by
         case MOE_EXPORT_ERROR: *offset = L.err; *bytes = 8; break;
         case MOE_EXPORT_POOL_ROWS: *offset = 0; *bytes = cap; break;
         case MOE_EXPORT_MAX_COUNT: *offset = L.max_count; *bytes = 4; break;
+        case MOE_EXPORT_X_Q: *offset = L.x_q; *bytes = static_cast<size_t>(ps->T) * ps->H; break;
         default: return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;

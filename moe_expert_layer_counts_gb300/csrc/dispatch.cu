@@ -7,8 +7,9 @@
 // The pages quantise upstream and move FP8 rows with 1-D TMA copies.  Here
 // the quantisation is fused into the gather: each token row is read once,
 // quantised once (E4M3 codes, one UE8M0 byte per 32 elements), and written to
-// each of its k pool rows.  One warp handles a 1024-element segment of one
-// token; a lane owns 16 consecutive elements (two 16-byte loads, one 16-byte
+// each of its k pool rows (or, when layer 1 gathers its rows by token, once
+// to a token-major copy, the pool rows getting only their scales).  One warp
+// handles a 1024-element segment of one token; a lane owns 16 consecutive elements (two 16-byte loads, one 16-byte
 // store per pool row), two lanes one 32-block.
 // Scales are written directly in the tensor-core layout the GEMM consumes:
 // chunk (row/128, col/128) of 512 bytes, byte 16*(row%32) + 4*((row%128)/32)
@@ -24,10 +25,13 @@ namespace {
 constexpr int kSeg = 1024;  // elements per warp work item
 constexpr int kThreads = 256;
 
+// x_q != nullptr: the token's codes go once to x_q[t] (token-major) and the
+// pool rows get only their scales; otherwise every pool row gets the codes.
 __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t* __restrict__ x, int T, int H, int k,
                                                                    const int* __restrict__ slot_of,
                                                                    uint8_t* __restrict__ pool_q,
-                                                                   uint8_t* __restrict__ pool_sf, int scale_rule) {
+                                                                   uint8_t* __restrict__ pool_sf, int scale_rule,
+                                                                   uint8_t* __restrict__ x_q) {
     const int lane = threadIdx.x & 31;
     const int nseg = (H + kSeg - 1) / kSeg;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
@@ -66,11 +70,12 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
         const uint32_t sw = __shfl_sync(0xffffffffu, sbyte, g) | (__shfl_sync(0xffffffffu, sbyte, g + 2) << 8) |
                             (__shfl_sync(0xffffffffu, sbyte, g + 4) << 16) |
                             (__shfl_sync(0xffffffffu, sbyte, g + 6) << 24);
+        if (x_q && active) *reinterpret_cast<uint4*>(x_q + static_cast<size_t>(t) * H + col) = codes;
         for (int j = 0; j < k; ++j) {
             const int r = __shfl_sync(0xffffffffu, my_slot, j);
             if (r < 0) continue;
             if (active) {
-                *reinterpret_cast<uint4*>(pool_q + static_cast<size_t>(r) * H + col) = codes;
+                if (!x_q) *reinterpret_cast<uint4*>(pool_q + static_cast<size_t>(r) * H + col) = codes;
                 if ((lane & 7) == 0) {
                     const size_t chunk = static_cast<size_t>(r / kBlockM) * sf_cols + col / 128;
                     const int m = r % kBlockM;
@@ -84,14 +89,15 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
 
 }  // namespace
 
-cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, cudaStream_t s) {
+cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, bool gather,
+                            cudaStream_t s) {
     if (L.T == 0) return cudaSuccess;
     const int nseg = (L.H + kSeg - 1) / kSeg;
     const int64_t items = static_cast<int64_t>(L.T) * nseg;
     const int64_t blocks = (items + kThreads / 32 - 1) / (kThreads / 32);
     dispatch_quant_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
         static_cast<const uint16_t*>(x), L.T, L.H, L.k, reinterpret_cast<const int*>(ws + L.slot_of),
-        ws + L.pool_q, ws + L.pool_sf, scale_rule);
+        ws + L.pool_q, ws + L.pool_sf, scale_rule, gather ? ws + L.x_q : nullptr);
     return cudaGetLastError();
 }
 

@@ -76,6 +76,7 @@ constexpr int kABoxLevels = 4;  // A boxes of 16, 32, 64 and 128 rows
 struct Maps {
     CUtensorMap box[kABoxLevels];  // A: boxes of 16, 32, 64 and 128 rows
     CUtensorMap out;               // layer 2 output: bf16 [P_cap][H], box 32 x 32, 64-byte swizzle
+    CUtensorMap gather;            // layer 1, gathered A: token-major x codes [T][H], box 128 K x 1 row
 };
 
 __device__ __forceinline__ int a_box_level(int rows) {
@@ -127,6 +128,7 @@ struct GemmParams {
     const int* block_rows;  // valid rows of each pool row block (plan)
     const int* max_count;   // largest expert count (plan): selects the ring shape
     const uint8_t* a_rows;  // A operand rows (pool or h), K bytes each
+    int a_gather;           // layer 1: A rows gathered by token (tile::gather4 from maps.gather)
 };
 
 // Work items are handed out by a global counter (dynamic scheduling: a CTA
@@ -450,7 +452,10 @@ __device__ __forceinline__ bool wait_l1_block(const int* counter, int target, Sh
 }
 
 // kMode 1 / 2: one layer; kMode 3: both layers in one persistent launch.
-template <int kMode, bool kClamp>
+// kGather: layer 1 gathers its A rows by token (the whole producer warp runs
+// the producer loop); otherwise one thread runs it alone (the broadcasts a
+// warp-wide loop needs cost 17% on the latency-bound operand stream).
+template <int kMode, bool kClamp, bool kGather>
 __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_constant__ KernelArgs ka) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
     extern __shared__ uint8_t smem_raw[];
@@ -495,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
             ptx::prefetch_tensormap(&ka.tmap_b[l]);
         }
         if (kMode != 1) ptx::prefetch_tensormap(&ka.maps[1].out);
+        if (kGather) ptx::prefetch_tensormap(&ka.maps[0].gather);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_addr(&sh->tmem_base), kTmemCols);
@@ -505,8 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&sh->tmem_base);
 
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && (kGather || lane == 0)) {
         // ------------------------------------------------ TMA producer
+        // Lane 0 takes every decision (waits, the work counter, the queue, all
+        // copies but one kind).  With gathered A rows the whole warp runs the
+        // loop in step, the decisions are broadcast, and lane l fetches rows
+        // 4l..4l+3 of a layer-1 block with one tile::gather4 load; otherwise
+        // lane 0 runs it alone and the broadcasts vanish.
+        const bool leader = lane == 0;
+        auto bcast = [&](int v) { return kGather ? __shfl_sync(0xffffffffu, v, 0) : v; };
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
@@ -521,13 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
         decode_item<kMode>(ka, w, n_work1, layer, b, j);
         int e = __ldg(p0.block_expert + b), rows = __ldg(p0.block_rows + b);
         bool all_l1_done = false;  // fused: every row block's layer-1 tiles seen complete
-        ok = put_item(sh, seq++, w, p0.err);
+        ok = bcast(leader ? put_item(sh, seq, w, p0.err) : true);
+        ++seq;
         while (ok) {
-            const int wn = min(n_work, static_cast<int>(gridDim.x) + atomicAdd(ka.work_ctr, 1));
-            if (!put_item(sh, seq++, wn, p0.err)) {
+            int wn = 0;
+            if (leader) wn = min(n_work, static_cast<int>(gridDim.x) + atomicAdd(ka.work_ctr, 1));
+            wn = bcast(wn);
+            if (!bcast(leader ? put_item(sh, seq, wn, p0.err) : true)) {
                 ok = false;
                 break;
             }
+            ++seq;
             int next_layer = 0, next_b = 0, next_j = 0, next_e = 0, next_rows = 0;
             if (wn < n_work) {
                 decode_item<kMode>(ka, wn, n_work1, next_layer, next_b, next_j);
@@ -538,13 +555,21 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
             const int kb_count = P.K / kBlockK;
             const int pairs = (P.N + 255) / 256;
             if (kMode == 3 && layer == 2 && !all_l1_done) {
-                if (ptx::ld_acquire_gpu(ka.blocks_done) >= n_blocks) {
-                    all_l1_done = true;
-                    ptx::fence_proxy_async_global();
-                } else if (!wait_l1_block(ka.l1_done + b, kEpiWarps * ka.p[0].n_tiles, sh, p0.err)) {
+                int st = 1;  // 1 ready, 2 all blocks done, 0 failed
+                if (leader) {
+                    if (ptx::ld_acquire_gpu(ka.blocks_done) >= n_blocks) {
+                        st = 2;
+                        ptx::fence_proxy_async_global();
+                    } else if (!wait_l1_block(ka.l1_done + b, kEpiWarps * ka.p[0].n_tiles, sh, p0.err)) {
+                        st = 0;
+                    }
+                }
+                st = bcast(st);
+                if (st == 0) {
                     ok = false;
                     break;
                 }
+                all_l1_done = st == 2;
             }
             // layer 1: gate|up halves of expert e, rows j*128 of each (3-D map: K, row, expert-half)
             // layer 2: rows e*H + 256*j .. +256 (2-D map)
@@ -552,27 +577,50 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
             const int b_z = layer == 1 ? 2 * e : 0;
             const uint8_t* sfa = P.sfa + static_cast<size_t>(b) * kb_count * kSfChunkBytes;
             const uint8_t* sfb = P.sfb + (static_cast<size_t>(e) * pairs + j) * kb_count * 2 * kSfChunkBytes;
+            const bool gather = kGather && layer == 1;
+            // gathered A: groups of 4 rows covering the block's valid rows; the
+            // token of a row (a padding row's token is -1: row 0 stands in, its
+            // accumulator row is never stored)
+            const int groups = (rows + 3) / 4;
+            int t0 = 0, t1 = 0, t2 = 0, t3 = 0;
+            if (gather && lane < groups) {
+                const int4 tk = __ldg(reinterpret_cast<const int4*>(p0.row_token + b * kBlockM) + lane);
+                t0 = max(tk.x, 0);
+                t1 = max(tk.y, 0);
+                t2 = max(tk.z, 0);
+                t3 = max(tk.w, 0);
+            }
             const int level = a_box_level(rows);  // the A box that covers the block's valid rows
-            const uint32_t tx = kStageTxBytes - (kBlockM - (16 << level)) * kBlockK;
+            const uint32_t a_tx = gather ? groups * 4 * kBlockK : (16u << level) * kBlockK;
+            const uint32_t tx = kStageTxBytes - kABytes + a_tx;
             const CUtensorMap* map_a = &ka.maps[layer - 1].box[level];
             const CUtensorMap* map_b = &ka.tmap_b[layer - 1];
             for (int kb = 0; kb < kb_count; ++kb) {
-                if (aborted(sh) ||
-                    !wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p0.err, stage, kWaitNs)) {
+                bool go = true;
+                if (leader)
+                    go = !aborted(sh) &&
+                         wait_or_abort(ptx::smem_addr(&sh->empty[stage]), phase ^ 1, sh, p0.err, stage, kWaitNs);
+                if (!bcast(go)) {
                     ok = false;
                     break;
                 }
                 uint8_t* st = ring + stage * stride;
                 const uint32_t full = ptx::smem_addr(&sh->full[stage]);
-                ptx::mbar_arrive_expect_tx(full, tx);
-                ptx::tma_load_2d(ptx::smem_addr(st), map_a, kb * kBlockK, b * kBlockM, full);
-                if (layer == 1)
-                    ptx::tma_load_3d(ptx::smem_addr(st + a_bytes), map_b, kb * kBlockK, b_y, b_z, full);
-                else
-                    ptx::tma_load_2d(ptx::smem_addr(st + a_bytes), map_b, kb * kBlockK, b_y, full);
-                ptx::bulk_load(ptx::smem_addr(st + sf_off), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
-                ptx::bulk_load(ptx::smem_addr(st + sf_off + kSfChunkBytes), sfb + kb * 2 * kSfChunkBytes,
-                               2 * kSfChunkBytes, full);
+                if (leader) {
+                    ptx::mbar_arrive_expect_tx(full, tx);
+                    if (!gather) ptx::tma_load_2d(ptx::smem_addr(st), map_a, kb * kBlockK, b * kBlockM, full);
+                    if (layer == 1)
+                        ptx::tma_load_3d(ptx::smem_addr(st + a_bytes), map_b, kb * kBlockK, b_y, b_z, full);
+                    else
+                        ptx::tma_load_2d(ptx::smem_addr(st + a_bytes), map_b, kb * kBlockK, b_y, full);
+                    ptx::bulk_load(ptx::smem_addr(st + sf_off), sfa + kb * kSfChunkBytes, kSfChunkBytes, full);
+                    ptx::bulk_load(ptx::smem_addr(st + sf_off + kSfChunkBytes), sfb + kb * 2 * kSfChunkBytes,
+                                   2 * kSfChunkBytes, full);
+                }
+                if (kGather) __syncwarp();
+                if (gather && lane < groups)
+                    ptx::tma_gather4(ptx::smem_addr(st + lane * 4 * kBlockK), &ka.maps[0].gather, kb * kBlockK, t0, t1,
+                                     t2, t3, full);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == n_stages) {
@@ -580,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
                     phase ^= 1;
                 }
             }
-            if (wn >= n_work) break;
+            if (!ok || wn >= n_work) break;
             w = wn;
             layer = next_layer;
             b = next_b;
@@ -588,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
             e = next_e;
             rows = next_rows;
         }
-        if (!ok) {
+        if (!ok && leader) {
             // let this CTA's copies in flight land before the CTA may exit
             for (int s = 0; s < n_stages; ++s)
                 if (issued_mask & (1u << s))
@@ -805,6 +853,21 @@ bool make_map_3d_fp4(CUtensorMap* map, const void* base, uint64_t k_elems, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token-major E4M3 rows [rows][cols] for tile::gather4 loads: box 128 columns x
+// 1 row, 128-byte swizzle (four gathered rows land as rows of the K-major,
+// 128-byte-swizzled A tile that the MMA reads).
+bool make_gather_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // bf16 [rows][cols] output map for tensor stores: box 32 columns x 32 rows,
 // 64-byte swizzle (the staging layout of store_out_rows).
 bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
@@ -826,7 +889,7 @@ namespace {
 // Opt a kernel into its dynamic shared memory once per device.
 template <typename Kernel>
 cudaError_t smem_attr_once(Kernel kernel, int slot, int bytes) {
-    static int done[5][64] = {};
+    static int done[9][64] = {};
     int dev = 0;
     cudaError_t st = cudaGetDevice(&dev);
     if (st != cudaSuccess) return st;
@@ -861,12 +924,15 @@ bool fill_layer(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, Ke
     p.fast_math = g.fast_math;
     Maps& maps = ka->maps[layer - 1];
     bool ok = true;
+    maps.gather = CUtensorMap{};  // used by layer 1 with gathered A rows only
     if (layer == 1) {
         p.a_rows = ws + L.pool_q;
         p.sfa = ws + L.pool_sf;
         p.out_q = ws + L.h_q;
         p.out_sf = ws + L.h_sf;
         p.n_tiles = L.I / 128;
+        p.a_gather = g.a_gather ? 1 : 0;
+        if (g.a_gather && !make_gather_map(&maps.gather, ws + L.x_q, L.H, L.T)) return false;
         maps.out = CUtensorMap{};  // unused by layer 1
         // W1 as [2E expert-halves][I rows][H]: 128 gate rows + the matching 128 up rows
         ok = make_map_3d_fp4(&ka->tmap_b[0], g.w_q, g.K, g.N / 2, 2 * static_cast<uint64_t>(g.E));
@@ -884,13 +950,25 @@ bool fill_layer(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, Ke
     return ok;
 }
 
-template <int kMode, bool kClamp>
+template <int kMode, bool kClamp, bool kGather>
 cudaError_t launch_mode(const KernelArgs& ka, int slot, int num_sms, cudaStream_t s) {
-    cudaError_t st = smem_attr_once(expert_gemm_kernel<kMode, kClamp>, slot, kSmemBytes);
+    cudaError_t st = smem_attr_once(expert_gemm_kernel<kMode, kClamp, kGather>, slot, kSmemBytes);
     if (st != cudaSuccess) return st;
     if (kMode != 3 && (st = cudaMemsetAsync(ka.work_ctr, 0, sizeof(int), s)) != cudaSuccess) return st;
-    expert_gemm_kernel<kMode, kClamp><<<num_sms, kThreads, kSmemBytes, s>>>(ka);
+    expert_gemm_kernel<kMode, kClamp, kGather><<<num_sms, kThreads, kSmemBytes, s>>>(ka);
     return cudaGetLastError();
+}
+
+// Layer 1 alone (kMode 1) or fused (kMode 3): the instantiation for the clamp
+// and the A operand's source.
+template <int kMode>
+cudaError_t launch_layer1_mode(const KernelArgs& ka, int slot0, int num_sms, cudaStream_t s) {
+    const bool clamp = ka.p[0].clamp != std::numeric_limits<float>::infinity();
+    if (ka.p[0].a_gather)
+        return clamp ? launch_mode<kMode, true, true>(ka, slot0 + 3, num_sms, s)
+                     : launch_mode<kMode, false, true>(ka, slot0 + 2, num_sms, s);
+    return clamp ? launch_mode<kMode, true, false>(ka, slot0 + 1, num_sms, s)
+                 : launch_mode<kMode, false, false>(ka, slot0, num_sms, s);
 }
 
 }  // namespace
@@ -901,9 +979,8 @@ cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const Ge
     KernelArgs ka{};
     if (!fill_layer(layer, L, ws, g, &ka)) return cudaErrorInvalidValue;
     ka.work_ctr = reinterpret_cast<int*>(ws + L.sched) + (layer - 1);
-    const bool clamp = ka.p[layer - 1].clamp != std::numeric_limits<float>::infinity();
-    if (layer == 1) return clamp ? launch_mode<1, true>(ka, 2, num_sms, s) : launch_mode<1, false>(ka, 0, num_sms, s);
-    return launch_mode<2, false>(ka, 1, num_sms, s);
+    if (layer == 1) return launch_layer1_mode<1>(ka, 0, num_sms, s);
+    return launch_mode<2, false, false>(ka, 4, num_sms, s);
 }
 
 cudaError_t launch_expert_fused(const Layout& L, uint8_t* ws, const GemmLaunch& g1, const GemmLaunch& g2, int num_sms,
@@ -922,8 +999,7 @@ cudaError_t launch_expert_fused(const Layout& L, uint8_t* ws, const GemmLaunch& 
     cudaError_t st = cudaMemsetAsync(ws + L.sched, 0, sizeof(int) * (kSchedWords + blocks), s);
     if (st != cudaSuccess) return st;
     if (!publish && (st = cudaMemsetAsync(ka.l1_done, 0x80, sizeof(int) * blocks, s)) != cudaSuccess) return st;
-    const bool clamp = ka.p[0].clamp != std::numeric_limits<float>::infinity();
-    return clamp ? launch_mode<3, true>(ka, 4, num_sms, s) : launch_mode<3, false>(ka, 3, num_sms, s);
+    return launch_layer1_mode<3>(ka, 5, num_sms, s);
 }
 
 }  // namespace moe

@@ -31,6 +31,7 @@ struct Layout {
     size_t err, n_blocks, max_count, count, off, poff, hist, chunk_base, block_expert, block_rows;
     size_t slot_of, row_token, row_topk, row_weight;
     size_t pool_q, pool_sf, h_q, h_sf, l2_out;
+    size_t x_q;        // token-major MXFP8 codes of x [T, H] (layer 1 gathers its rows from here)
     size_t sched;      // expert kernels: work counters (L1, L2, fused), then per row block the
                        // layer-1 epilogue warps done (fused kernel's readiness counters)
     size_t total;
@@ -51,7 +52,10 @@ constexpr uint64_t kPlanMagic = 0x4D6F45506C616E31ull;  // "MoEPlan1"
 // Launchers (enqueue only; return cudaError_t of the launch).
 cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, const float* topk_w,
                          cudaStream_t s);
-cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, cudaStream_t s);
+// gather: write each token's codes once, token-major, instead of the pool rows
+// (the pool's scales are written either way).
+cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, bool gather,
+                            cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s);
 cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves, uint8_t* out, size_t out_bytes,
                               cudaStream_t s);
@@ -66,6 +70,7 @@ struct GemmLaunch {
     float clamp;          // layer 1: limit of the bf16 gate/up values (0 = none)
     int scale_rule;       // layer 1: MOE_SCALE_CEIL or MOE_SCALE_OCP_FLOOR for h
     int fast_math;        // layer 1: 1 = fast SwiGLU with exact decisions, 0 = exact everywhere
+    bool a_gather;        // layer 1: A rows gathered by token from token-major x (tile::gather4)
 };
 // layer 1: pool x W1 -> requantised h; layer 2: h x W2 -> bf16 rows.
 cudaError_t launch_expert_gemm(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, int num_sms,

@@ -70,7 +70,7 @@ def test_argument_errors_before_any_device_call(libmoe):
     import moe_expert_layer_counts_gb300 as moe
     assert ctypes.sizeof(moe.Options) == 32
     for bad in (moe.Options(scale_rule=2), moe.Options(fast_math=3), moe.Options(activation_clamp=-1.0),
-                moe.Options(activation_clamp=float("nan"))):
+                moe.Options(activation_clamp=float("nan")), moe.Options(a_operand=2)):
         assert libmoe.moe_forward(None, None, None, plan, None, ctypes.addressof(bad), None) == 1
     libmoe.moe_error_string.restype = ctypes.c_char_p
     for s in range(8):
