@@ -128,7 +128,7 @@ bool make_layout(int T, int k, int E, int H, int I, Layout* L) {
         o = align_up(o + bytes, 1024);
         return at;
     };
-    L->err = take(2 * sizeof(int));
+    L->err = take(kErrWords * sizeof(int));
     L->n_blocks = take(sizeof(int));
     L->max_count = take(sizeof(int));  // largest expert count (selects the GEMM's operand ring)
     L->count = take(sizeof(int) * E);

@@ -22,6 +22,10 @@ constexpr int kSchedWords = 4;         // work counters at the head of the sched
 // where a bounded wait expired.
 constexpr int kDevErrBadExpert = 1;
 constexpr int kDevErrTimeout = 2;
+// The error record's region: words 0-1 the record, words 4-7 the scheduling
+// words of the one-launch plan kernel (zeroed together before each plan).
+constexpr int kErrWords = 8;
+constexpr int kErrSyncOff = 4;
 
 // Byte offsets of every array inside the caller's workspace.
 struct Layout {

@@ -25,6 +25,7 @@
 // single launch.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "internal.h"
@@ -47,6 +48,17 @@ __host__ __device__ constexpr int small_threads(int E) {
                : (kSmallSmemInts / E - 3) * 32 < kSmallMinThreads ? kSmallMinThreads : (kSmallSmemInts / E - 3) * 32;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ int ld_acquire_gpu_int(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
@@ -64,14 +76,13 @@ __device__ __forceinline__ int entry_expert(const int64_t* idx, int64_t i, int64
     return static_cast<int>(v);
 }
 
-__global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int64_t* __restrict__ topk_idx,
-                                                                     int64_t n_entries, int E,
-                                                                     int* __restrict__ hist, int* __restrict__ err) {
-    extern __shared__ int s_hist[];
+// Histogram of chunk `chunk` (kRouteChunk entries) into hist[chunk][E].
+__device__ __forceinline__ void count_chunk(const int64_t* __restrict__ topk_idx, int64_t n_entries, int E, int chunk,
+                                            int* __restrict__ hist, int* __restrict__ err, int* s_hist) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+    const int64_t base = static_cast<int64_t>(chunk) * kRouteChunk;
     const int64_t end = min(base + kRouteChunk, n_entries);
     bool bad = false;
     for (int64_t i0 = base; i0 < end; i0 += blockDim.x) {
@@ -81,7 +92,14 @@ __global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int64_
     }
     if (bad) atomicOr(err, kDevErrBadExpert);
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(blockIdx.x) * E + e] = s_hist[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<size_t>(chunk) * E + e] = s_hist[e];
+}
+
+__global__ void __launch_bounds__(kCountThreads) route_count_kernel(const int64_t* __restrict__ topk_idx,
+                                                                     int64_t n_entries, int E,
+                                                                     int* __restrict__ hist, int* __restrict__ err) {
+    extern __shared__ int s_hist[];
+    count_chunk(topk_idx, n_entries, E, blockIdx.x, hist, err, s_hist);
 }
 
 // Block-wide inclusive scan of one int per thread (blockDim.x == 1024).
@@ -109,7 +127,11 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int* s_warp) {
     return r;
 }
 
-__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __restrict__ hist, int chunks, int E,
+// The prefix sums over chunks and experts (one thread per expert; blockDim.x ==
+// kScanThreads): counts, exclusive scans of counts and of padded counts, each
+// chunk's base per expert, the row-block tables, the largest count and the
+// padding rows' inverse maps.
+__device__ __forceinline__ void scan_body(const int* __restrict__ hist, int chunks, int E,
                                                                    int* __restrict__ count, int* __restrict__ off,
                                                                    int* __restrict__ poff,
                                                                    int* __restrict__ chunk_base,
@@ -176,22 +198,40 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
     }
 }
 
-__global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
-    const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
-    const int* __restrict__ poff, const int* __restrict__ chunk_base,
-    int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
-    float* __restrict__ row_weight) {
-    extern __shared__ int s_mem[];
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __restrict__ hist, int chunks, int E,
+                                                                   int* __restrict__ count, int* __restrict__ off,
+                                                                   int* __restrict__ poff,
+                                                                   int* __restrict__ chunk_base,
+                                                                   int* __restrict__ block_expert,
+                                                                   int* __restrict__ block_rows,
+                                                                   int* __restrict__ n_blocks,
+                                                                   int* __restrict__ max_count,
+                                                                   int* __restrict__ row_token,
+                                                                   int* __restrict__ row_topk,
+                                                                   float* __restrict__ row_weight) {
+    scan_body(hist, chunks, E, count, off, poff, chunk_base, block_expert, block_rows, n_blocks, max_count, row_token,
+              row_topk, row_weight);
+}
+
+// Stable slots of chunk `chunk`: ranks inside the chunk in flat order (rank in
+// warp from the match mask, plus same-expert counts of lower warps) on top of
+// the expert's padded offset and the chunk's base; inverse maps of every
+// routed pool row.  s_mem: E * (1 + warps) ints.
+__device__ __forceinline__ void slot_chunk(const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
+                                           int64_t n_entries, int k, int E, int chunk, const int* __restrict__ poff,
+                                           const int* __restrict__ chunk_base, int* __restrict__ slot_of,
+                                           int* __restrict__ row_token, int* __restrict__ row_topk,
+                                           float* __restrict__ row_weight, int* s_mem) {
     const int nwarps = blockDim.x / 32;
     int* s_next = s_mem;        // [E] next free slot of each expert for this chunk
     int* s_wcnt = s_mem + E;    // [nwarps][E] same-expert counts per warp, this round
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        s_next[e] = poff[e] + chunk_base[static_cast<size_t>(blockIdx.x) * E + e];
+        s_next[e] = poff[e] + chunk_base[static_cast<size_t>(chunk) * E + e];
         for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
     }
     __syncthreads();
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+    const int64_t base = static_cast<int64_t>(chunk) * kRouteChunk;
     const int64_t end = min(base + kRouteChunk, n_entries);
     bool bad = false;
     for (int64_t i0 = base; i0 < end; i0 += blockDim.x) {
@@ -221,6 +261,95 @@ __global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
                 row_weight[slot] = __ldg(topk_w + i);
             }
         }
+    }
+}
+
+__global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
+    const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
+    const int* __restrict__ poff, const int* __restrict__ chunk_base,
+    int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
+    float* __restrict__ row_weight) {
+    extern __shared__ int s_mem[];
+    slot_chunk(topk_idx, topk_w, n_entries, k, E, blockIdx.x, poff, chunk_base, slot_of, row_token, row_topk,
+               row_weight, s_mem);
+}
+
+// The whole plan in ONE multi-CTA launch for batches of more than one chunk
+// and at most kFusedMaxExperts experts.  Three phases over the chunks, each
+// chunk taken from a work counter (sync[0], sync[1]):
+//   1. histograms of chunks; the CTA that counts the last chunk done (sync[2])
+//   2. runs the scans (as route_scan) and releases a flag (sync[3]);
+//   3. every CTA then takes chunks for the stable slots (as route_slot).
+// A CTA waits for the flag only once no chunk of phase 1 is left to take, so
+// every chunk of phase 1 is held by a running CTA: no co-residency is needed.
+// The wait is bounded (1 s of global time; the error record gets
+// MOE_ERR_TIMEOUT).  sync[0..3] must be zero at launch.
+constexpr int kFusedMaxExperts = 256;
+constexpr uint64_t kRouteWaitNs = 1000000000ull;
+
+__global__ void __launch_bounds__(kScanThreads) route_fused_kernel(
+    const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
+    int chunks, int* __restrict__ sync, int* __restrict__ hist, int* __restrict__ count, int* __restrict__ off,
+    int* __restrict__ poff, int* __restrict__ chunk_base, int* __restrict__ block_expert,
+    int* __restrict__ block_rows, int* __restrict__ n_blocks, int* __restrict__ max_count,
+    int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
+    float* __restrict__ row_weight, int* __restrict__ err) {
+    extern __shared__ int s_mem[];
+    __shared__ int s_chunk, s_last;
+    // 1. counts
+    while (true) {
+        if (threadIdx.x == 0) s_chunk = atomicAdd(&sync[0], 1);
+        __syncthreads();
+        const int c = s_chunk;
+        __syncthreads();
+        if (c >= chunks) break;
+        count_chunk(topk_idx, n_entries, E, c, hist, err, s_mem);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();  // this chunk's histogram before the count of finished chunks
+            s_last = atomicAdd(&sync[2], 1) == chunks - 1;
+        }
+        __syncthreads();
+        if (s_last) {
+            // 2. the last chunk is in: every histogram is visible
+            __threadfence();
+            scan_body(hist, chunks, E, count, off, poff, chunk_base, block_expert, block_rows, n_blocks, max_count,
+                      row_token, row_topk, row_weight);
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicExch(&sync[3], 1);
+            }
+        }
+    }
+    // 3. stable slots, once the scans are released
+    if (threadIdx.x == 0) {
+        const uint64_t deadline = globaltimer_ns() + kRouteWaitNs;
+        bool ok = true;
+        while (ld_acquire_gpu_int(&sync[3]) == 0) {
+            if (globaltimer_ns() > deadline) {
+                ok = false;
+                break;
+            }
+            __nanosleep(256);
+        }
+        if (!ok) {
+            atomicOr(err, kDevErrTimeout);
+            atomicCAS(err + 1, 0, 1 + 99);
+        }
+        s_last = ok;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    while (true) {
+        if (threadIdx.x == 0) s_chunk = atomicAdd(&sync[1], 1);
+        __syncthreads();
+        const int c = s_chunk;
+        __syncthreads();
+        if (c >= chunks) break;
+        slot_chunk(topk_idx, topk_w, n_entries, k, E, c, poff, chunk_base, slot_of, row_token, row_topk, row_weight,
+                   s_mem);
+        __syncthreads();
     }
 }
 
@@ -368,8 +497,19 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
             reinterpret_cast<int*>(ws + L.row_topk), reinterpret_cast<float*>(ws + L.row_weight), err);
         return cudaGetLastError();
     }
-    cudaError_t st = cudaMemsetAsync(err, 0, 2 * sizeof(int), s);
+    // the error record and the fused plan's four scheduling words start at zero
+    cudaError_t st = cudaMemsetAsync(err, 0, kErrWords * sizeof(int), s);
     if (st != cudaSuccess) return st;
+    if (L.E <= kFusedMaxExperts && L.chunks > 0) {  // the whole plan in one launch
+        const size_t smem = static_cast<size_t>(L.E) * (1 + kScanThreads / 32) * sizeof(int);
+        route_fused_kernel<<<std::min(L.chunks, 512), kScanThreads, smem, s>>>(
+            topk_idx, topk_w, n, L.k, L.E, L.chunks, err + kErrSyncOff, hist, count, off, poff, chunk_base,
+            reinterpret_cast<int*>(ws + L.block_expert), reinterpret_cast<int*>(ws + L.block_rows),
+            reinterpret_cast<int*>(ws + L.n_blocks), reinterpret_cast<int*>(ws + L.max_count),
+            reinterpret_cast<int*>(ws + L.slot_of), reinterpret_cast<int*>(ws + L.row_token),
+            reinterpret_cast<int*>(ws + L.row_topk), reinterpret_cast<float*>(ws + L.row_weight), err);
+        return cudaGetLastError();
+    }
     if (L.chunks > 0) {
         route_count_kernel<<<L.chunks, kCountThreads, L.E * sizeof(int), s>>>(topk_idx, n, L.E, hist, err);
         if ((st = cudaGetLastError()) != cudaSuccess) return st;
