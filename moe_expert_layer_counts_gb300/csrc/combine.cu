@@ -6,9 +6,12 @@
 // y[t] = bf16( sum over ascending j of the valid entries' L2 rows ), summed
 // in fp32 starting from 0, one rounding at the end; tokens without a valid
 // entry get +0.  The top-k weight was applied once, in the L1 epilogue.
-// One warp handles a 1024-element segment of one token; a lane owns 8
-// consecutive elements (one 16-byte load per source row), and up to 8 source
-// rows are loaded before they are added, so the loads overlap.
+// One warp handles a 1024-element segment of one token; a lane owns four
+// 8-element chunks of it (one 16-byte load per chunk and source row).  The
+// warp reads only the rows of the token's valid entries (a bit mask of them,
+// taken in ascending j), two rows per round with all their chunks loaded
+// before they are added, so a warp keeps 8 loads in flight whether the token
+// has one valid entry (an expert-parallel shard) or all k.
 #include <cuda_runtime.h>
 
 #include "formats.cuh"
@@ -18,7 +21,19 @@ namespace moe {
 namespace {
 
 constexpr int kSeg = 1024;
+constexpr int kChunks = kSeg / 256;
 constexpr int kThreads = 256;
+
+__device__ __forceinline__ void add8(float (&acc)[8], uint4 v) {
+    acc[0] += bf16_lo(v.x);
+    acc[1] += bf16_hi(v.x);
+    acc[2] += bf16_lo(v.y);
+    acc[3] += bf16_hi(v.y);
+    acc[4] += bf16_lo(v.z);
+    acc[5] += bf16_hi(v.z);
+    acc[6] += bf16_lo(v.w);
+    acc[7] += bf16_hi(v.w);
+}
 
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ rows,
                                                             const int* __restrict__ slot_of, int T, int H, int k,
@@ -30,45 +45,54 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
     if (t >= T) return;
     const int seg = static_cast<int>(item % nseg);
     const int my_slot = lane < k ? __ldg(slot_of + static_cast<size_t>(t) * k + lane) : -1;
+    // the token's valid entries, bit j for entry j: only those rows are read,
+    // in ascending j (the order of the sum)
+    const uint32_t valid = __ballot_sync(0xffffffffu, my_slot >= 0);
     const int s_begin = seg * kSeg, s_end = min(s_begin + kSeg, H);
-    for (int s0 = s_begin; s0 < s_end; s0 += 256) {
-        const int col = s0 + lane * 8;
-        const bool active = col < s_end;
-        float acc[8];
+    // chunk c of the segment: elements s_begin + 256c + 8*lane .. +7
+    bool active[kChunks];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int j0 = 0; j0 < k; j0 += 8) {
-            int r[8];
-            uint4 v[8];
+    for (int c = 0; c < kChunks; ++c) active[c] = s_begin + c * 256 + lane * 8 < s_end;
+    const size_t base = static_cast<size_t>(s_begin) + lane * 8;
+    float acc[kChunks][8];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) r[jj] = __shfl_sync(0xffffffffu, my_slot, (j0 + jj) & 31);
+    for (int c = 0; c < kChunks; ++c)
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                v[jj] = make_uint4(0, 0, 0, 0);
-                if (j0 + jj < k && r[jj] >= 0 && active)
-                    v[jj] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<size_t>(r[jj]) * H + col));
-            }
+        for (int i = 0; i < 8; ++i) acc[c][i] = 0.0f;
+    // two valid entries per round, all chunks of both rows loaded before they
+    // are added (8 loads in flight), the earlier entry added first
+    uint32_t m = valid;
+    while (m) {
+        const int j0 = __ffs(m) - 1;
+        m &= m - 1;
+        const int j1 = __ffs(m) - 1;  // -1: no second entry this round
+        if (m) m &= m - 1;
+        const bool two = j1 >= 0;
+        const uint16_t* r0 = rows + static_cast<size_t>(__shfl_sync(0xffffffffu, my_slot, j0)) * H + base;
+        const uint16_t* r1 = rows + static_cast<size_t>(max(__shfl_sync(0xffffffffu, my_slot, j1 & 31), 0)) * H + base;
+        uint4 v0[kChunks], v1[kChunks];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                if (j0 + jj < k && r[jj] >= 0) {
-                    acc[0] += bf16_lo(v[jj].x);
-                    acc[1] += bf16_hi(v[jj].x);
-                    acc[2] += bf16_lo(v[jj].y);
-                    acc[3] += bf16_hi(v[jj].y);
-                    acc[4] += bf16_lo(v[jj].z);
-                    acc[5] += bf16_hi(v[jj].z);
-                    acc[6] += bf16_lo(v[jj].w);
-                    acc[7] += bf16_hi(v[jj].w);
-                }
-            }
+        for (int c = 0; c < kChunks; ++c) {
+            v0[c] = make_uint4(0, 0, 0, 0);
+            v1[c] = make_uint4(0, 0, 0, 0);
+            if (active[c]) v0[c] = __ldg(reinterpret_cast<const uint4*>(r0 + c * 256));
+            if (active[c] && two) v1[c] = __ldg(reinterpret_cast<const uint4*>(r1 + c * 256));
         }
-        if (active) {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+            add8(acc[c], v0[c]);
+            if (two) add8(acc[c], v1[c]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        if (active[c]) {
             uint4 o;
-            o.x = bf16x2_rn(acc[0], acc[1]);
-            o.y = bf16x2_rn(acc[2], acc[3]);
-            o.z = bf16x2_rn(acc[4], acc[5]);
-            o.w = bf16x2_rn(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + col) = o;
+            o.x = bf16x2_rn(acc[c][0], acc[c][1]);
+            o.y = bf16x2_rn(acc[c][2], acc[c][3]);
+            o.z = bf16x2_rn(acc[c][4], acc[c][5]);
+            o.w = bf16x2_rn(acc[c][6], acc[c][7]);
+            *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + base + c * 256) = o;
         }
     }
 }

@@ -23,6 +23,7 @@ namespace moe {
 namespace {
 
 constexpr int kSeg = 1024;  // elements per warp work item
+constexpr int kHalves = kSeg / 512;
 constexpr int kThreads = 256;
 
 // x_q != nullptr: the token's codes go once to x_q[t] (token-major) and the
@@ -41,15 +42,25 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
     const int my_slot = lane < k ? __ldg(slot_of + static_cast<size_t>(t) * k + lane) : -1;
     const int s_begin = seg * kSeg, s_end = min(s_begin + kSeg, H);
     const int sf_cols = H / 128;
-    for (int s0 = s_begin; s0 < s_end; s0 += 512) {
-        const int col = s0 + lane * 16;
-        const bool active = col < s_end;  // H is a multiple of 128: a lane's 16 columns are all in or all out
-        uint4 raw0 = make_uint4(0, 0, 0, 0), raw1 = make_uint4(0, 0, 0, 0);
-        if (active) {
+    // both 512-element halves of the segment are loaded before either is
+    // quantised (four 16-byte loads in flight per lane)
+    uint4 raw[kHalves][2];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+        raw[h][0] = make_uint4(0, 0, 0, 0);
+        raw[h][1] = make_uint4(0, 0, 0, 0);
+        const int col = s_begin + h * 512 + lane * 16;
+        if (col < s_end) {
             const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H + col);
-            raw0 = __ldg(src);
-            raw1 = __ldg(src + 1);
+            raw[h][0] = __ldg(src);
+            raw[h][1] = __ldg(src + 1);
         }
+    }
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h) {
+        const int col = s_begin + h * 512 + lane * 16;
+        const bool active = col < s_end;  // H is a multiple of 128: a lane's 16 columns are all in or all out
+        const uint4 raw0 = raw[h][0], raw1 = raw[h][1];
         float f[16] = {bf16_lo(raw0.x), bf16_hi(raw0.x), bf16_lo(raw0.y), bf16_hi(raw0.y),
                        bf16_lo(raw0.z), bf16_hi(raw0.z), bf16_lo(raw0.w), bf16_hi(raw0.w),
                        bf16_lo(raw1.x), bf16_hi(raw1.x), bf16_lo(raw1.y), bf16_hi(raw1.y),
