@@ -1,9 +1,9 @@
 """Benchmark of the fused MoE layer forward on GB300.
 
 One step = the whole hot path on one batch: moe_plan (one kernel:
-route_small for at most 2048 top-k entries, route_fused for up to 256
-experts) + moe_forward (dispatch_quant, the fused expert kernel, combine), on
-the full
+route_fused for up to 256 experts, route_small for more experts and at most
+2048 top-k entries) + moe_forward (dispatch_quant, the fused expert kernel,
+combine), on the full
 skewed workload T=8192, H=7168, I=2048, E=256, k=8 by default.  Inputs are
 synthetic and seeded, resident in HBM before timing; L2 is flushed (a 512 MB
 buffer is written) before every timed step, outside the timed events.
@@ -41,17 +41,18 @@ from moe_expert_layer_counts_gb300 import inputs  # noqa: E402
 METRIC = "MoE fwd TFLOP/s & tokens/s (T=8192,H=7168,I=2048,E=256,k=8); % FP8 peak"
 STAGES = ("route", "dispatch", "experts", "combine")             # what moe_forward runs (fused expert kernel)
 STAGES_SEPARATE = ("route", "dispatch", "expert_l1", "expert_l2", "combine")
-ROUTE_CHUNK = 2048  # top-k entries the one-CTA plan handles
-FUSED_PLAN_EXPERTS = 256  # experts up to which a larger plan is one multi-CTA launch
+ROUTE_CHUNK = 2048  # top-k entries the one-CTA plan (more than 256 experts) handles
+FUSED_PLAN_EXPERTS = 256  # experts up to which the plan is one multi-CTA launch
 FLUSH_BYTES = 512 << 20
 # FLOPs of one oracle sample (about 7 s on 16 host cores at the full layer size)
 ORACLE_SAMPLE_FLOP = 4.0e11
 
 
 def kernels_per_step(w, fused=True) -> int:
-    """Kernels of the library one step launches: the plan (route_small for at
-    most ROUTE_CHUNK top-k entries, route_fused for up to FUSED_PLAN_EXPERTS
-    experts, otherwise route_count, route_scan and route_slot), dispatch_quant,
+    """Kernels of the library one step launches: the plan (route_fused for up
+    to FUSED_PLAN_EXPERTS experts, route_small for more experts and at most
+    ROUTE_CHUNK top-k entries, otherwise route_count, route_scan and
+    route_slot), dispatch_quant,
     the expert kernel(s) and combine.  Counters are zeroed by memset nodes,
     not kernels of the library."""
     one = w.T * w.k <= ROUTE_CHUNK or w.E <= FUSED_PLAN_EXPERTS

@@ -213,10 +213,65 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(const int* __r
               row_topk, row_weight);
 }
 
-// Stable slots of chunk `chunk`: ranks inside the chunk in flat order (rank in
-// warp from the match mask, plus same-expert counts of lower warps) on top of
-// the expert's padded offset and the chunk's base; inverse maps of every
-// routed pool row.  s_mem: E * (1 + warps) ints.
+// One round of stable ranks: the slot of this thread's entry (expert e, -1
+// for none) is s_next[e] + the same-expert entries of lower lanes of its warp
+// (match mask) + those of lower warps (s_wcnt, zero on entry and on exit);
+// s_next then advances past the round.  All threads of the CTA take part.
+__device__ __forceinline__ int rank_round(int e, int E, int* s_next, int* s_wcnt) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const bool leader = lane == __ffs(same) - 1;
+    if (e >= 0 && leader) s_wcnt[warp * E + e] = __popc(same);
+    __syncthreads();
+    int slot = -1;
+    if (e >= 0) {
+        int before = __popc(same & lanemask_lt());
+        for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
+        slot = s_next[e] + before;
+    }
+    __syncthreads();
+    if (e >= 0 && leader) {
+        atomicAdd(&s_next[e], __popc(same));
+        s_wcnt[warp * E + e] = 0;
+    }
+    __syncthreads();
+    return slot;
+}
+
+// The slot of entry i and the inverse maps of its pool row.
+__device__ __forceinline__ void write_slot(int64_t i, int slot, float w, int k, int* __restrict__ slot_of,
+                                           int* __restrict__ row_token, int* __restrict__ row_topk,
+                                           float* __restrict__ row_weight) {
+    slot_of[i] = slot;
+    if (slot >= 0) {
+        const int t = static_cast<int>(i) / k;  // plans hold at most 2^28 entries
+        row_token[slot] = t;
+        row_topk[slot] = static_cast<int>(i) - t * k;
+        row_weight[slot] = w;
+    }
+}
+
+// Stable slots of chunk `chunk`: ranks inside the chunk in flat order on top
+// of s_next[e] (the expert's padded offset plus the chunk's base, set by the
+// caller, with s_wcnt zeroed); inverse maps of every routed pool row.
+// s_wcnt: [warps][E] same-expert counts per warp, this round.
+__device__ __forceinline__ void slot_rank(const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
+                                          int64_t n_entries, int k, int E, int chunk, int* s_next, int* s_wcnt,
+                                          int* __restrict__ slot_of, int* __restrict__ row_token,
+                                          int* __restrict__ row_topk, float* __restrict__ row_weight) {
+    const int64_t base = static_cast<int64_t>(chunk) * kRouteChunk;
+    const int64_t end = min(base + kRouteChunk, n_entries);
+    bool bad = false;
+    for (int64_t i0 = base; i0 < end; i0 += blockDim.x) {
+        const int64_t i = i0 + threadIdx.x;
+        const int e = entry_expert(topk_idx, i, end, E, &bad);
+        const int slot = rank_round(e, E, s_next, s_wcnt);
+        if (i < end) write_slot(i, slot, __ldg(topk_w + i), k, slot_of, row_token, row_topk, row_weight);
+    }
+}
+
+// slot_rank of chunk `chunk` with the bases from the scan's tables.
+// s_mem: E * (1 + warps) ints.
 __device__ __forceinline__ void slot_chunk(const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
                                            int64_t n_entries, int k, int E, int chunk, const int* __restrict__ poff,
                                            const int* __restrict__ chunk_base, int* __restrict__ slot_of,
@@ -224,44 +279,13 @@ __device__ __forceinline__ void slot_chunk(const int64_t* __restrict__ topk_idx,
                                            float* __restrict__ row_weight, int* s_mem) {
     const int nwarps = blockDim.x / 32;
     int* s_next = s_mem;        // [E] next free slot of each expert for this chunk
-    int* s_wcnt = s_mem + E;    // [nwarps][E] same-expert counts per warp, this round
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int* s_wcnt = s_mem + E;    // [nwarps][E]
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         s_next[e] = poff[e] + chunk_base[static_cast<size_t>(chunk) * E + e];
         for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
     }
     __syncthreads();
-    const int64_t base = static_cast<int64_t>(chunk) * kRouteChunk;
-    const int64_t end = min(base + kRouteChunk, n_entries);
-    bool bad = false;
-    for (int64_t i0 = base; i0 < end; i0 += blockDim.x) {
-        const int64_t i = i0 + threadIdx.x;
-        const int e = entry_expert(topk_idx, i, end, E, &bad);
-        const uint32_t same = __match_any_sync(0xffffffffu, e);
-        const bool leader = lane == __ffs(same) - 1;
-        if (e >= 0 && leader) s_wcnt[warp * E + e] = __popc(same);
-        __syncthreads();
-        int slot = -1;
-        if (e >= 0) {
-            int before = __popc(same & lanemask_lt());
-            for (int w = 0; w < warp; ++w) before += s_wcnt[w * E + e];
-            slot = s_next[e] + before;
-        }
-        __syncthreads();
-        if (e >= 0 && leader) {
-            atomicAdd(&s_next[e], __popc(same));
-            s_wcnt[warp * E + e] = 0;
-        }
-        __syncthreads();
-        if (i < end) {
-            slot_of[i] = slot;
-            if (slot >= 0) {
-                row_token[slot] = static_cast<int>(i / k);
-                row_topk[slot] = static_cast<int>(i % k);
-                row_weight[slot] = __ldg(topk_w + i);
-            }
-        }
-    }
+    slot_rank(topk_idx, topk_w, n_entries, k, E, chunk, s_next, s_wcnt, slot_of, row_token, row_topk, row_weight);
 }
 
 __global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
@@ -274,82 +298,240 @@ __global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
                row_weight, s_mem);
 }
 
-// The whole plan in ONE multi-CTA launch for batches of more than one chunk
-// and at most kFusedMaxExperts experts.  Three phases over the chunks, each
-// chunk taken from a work counter (sync[0], sync[1]):
-//   1. histograms of chunks; the CTA that counts the last chunk done (sync[2])
-//   2. runs the scans (as route_scan) and releases a flag (sync[3]);
-//   3. every CTA then takes chunks for the stable slots (as route_slot).
-// A CTA waits for the flag only once no chunk of phase 1 is left to take, so
-// every chunk of phase 1 is held by a running CTA: no co-residency is needed.
-// The wait is bounded (1 s of global time; the error record gets
-// MOE_ERR_TIMEOUT).  sync[0..3] must be zero at launch.
+// The whole plan in ONE multi-CTA launch, for at most kFusedMaxExperts
+// experts and any number of entries:
+//   1. histograms of chunks, each chunk taken from a work counter (sync[0]);
+//      a finished chunk is counted in sync[2] (release);
+//   2. once sync[2] reaches the number of chunks (acquire), EVERY CTA sums the
+//      histogram rows itself (the per-expert totals, and the base of the slot
+//      chunk it takes next from sync[1]) and scans the totals, so no CTA waits
+//      for another's scan; CTA 0 writes the count / offset tables, and the
+//      row-block tables and padding rows are shared out one expert per warp
+//      over the whole grid;
+//   3. stable slots of the chunks taken from sync[1], as route_slot.
+// A CTA waits only once no chunk of phase 1 is left to take, so every chunk
+// of phase 1 is held by a running CTA: no co-residency is needed.  The wait
+// is bounded (1 s of global time; the error record gets MOE_ERR_TIMEOUT).
+// sync[0..3] must be zero at launch.
 constexpr int kFusedMaxExperts = 256;
+constexpr int kFusedMinCtas = 16;  // CTAs that share the tables and padding rows of a small batch
 constexpr uint64_t kRouteWaitNs = 1000000000ull;
+
+// Per-expert sums of the histogram rows of all chunks (s_tot) and of chunks
+// [0, upto) (s_base).  min(blockDim.x / E, 32) threads share an expert, each
+// summing a stride of the chunks; rows written by other CTAs are read at L2.
+// s_part: 2 * blockDim.x ints.
+__device__ __forceinline__ void chunk_sums(const int* __restrict__ hist, int chunks, int E, int upto, int* s_part,
+                                           int* s_tot, int* s_base) {
+    const int parts = min(static_cast<int>(blockDim.x) / E, 32);
+    const int e = threadIdx.x % E, part = threadIdx.x / E;
+    if (part < parts) {
+        int tot = 0, base = 0;
+#pragma unroll 8
+        for (int c = part; c < chunks; c += parts) {
+            const int v = __ldcg(hist + static_cast<size_t>(c) * E + e);
+            tot += v;
+            base += c < upto ? v : 0;
+        }
+        s_part[part * E + e] = tot;
+        s_part[(parts + part) * E + e] = base;
+    }
+    __syncthreads();
+    if (threadIdx.x < E) {
+        int tot = 0, base = 0;
+        for (int q = 0; q < parts; ++q) {
+            tot += s_part[q * E + threadIdx.x];
+            base += s_part[(parts + q) * E + threadIdx.x];
+        }
+        s_tot[threadIdx.x] = tot;
+        s_base[threadIdx.x] = base;
+    }
+    __syncthreads();
+}
+
+// Inclusive scans of two ints per thread at once (blockDim.x == 1024): packed
+// into one 64-bit sum, which cannot carry from the low half while the low
+// values sum to less than 2^32.
+__device__ __forceinline__ void block_inclusive_scan2(int a, int b, int* s_warp2, int& inc_a, int& inc_b) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t v = (static_cast<uint64_t>(static_cast<uint32_t>(b)) << 32) | static_cast<uint32_t>(a);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint64_t o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += o;
+    }
+    uint64_t* s_w = reinterpret_cast<uint64_t*>(s_warp2);
+    if (lane == 31) s_w[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t w = s_w[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint64_t o = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += o;
+        }
+        s_w[lane] = w;
+    }
+    __syncthreads();
+    const uint64_t r = v + (warp > 0 ? s_w[warp - 1] : 0ull);
+    inc_a = static_cast<int>(static_cast<uint32_t>(r));
+    inc_b = static_cast<int>(r >> 32);
+}
+
+constexpr int kFusedPer = kRouteChunk / kScanThreads;  // entries of a chunk per thread
+static_assert(kFusedPer * kScanThreads == kRouteChunk, "a chunk is whole rounds of the plan CTA");
 
 __global__ void __launch_bounds__(kScanThreads) route_fused_kernel(
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
     int chunks, int* __restrict__ sync, int* __restrict__ hist, int* __restrict__ count, int* __restrict__ off,
-    int* __restrict__ poff, int* __restrict__ chunk_base, int* __restrict__ block_expert,
-    int* __restrict__ block_rows, int* __restrict__ n_blocks, int* __restrict__ max_count,
-    int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
-    float* __restrict__ row_weight, int* __restrict__ err) {
+    int* __restrict__ poff, int* __restrict__ block_expert, int* __restrict__ block_rows,
+    int* __restrict__ n_blocks, int* __restrict__ max_count, int* __restrict__ slot_of,
+    int* __restrict__ row_token, int* __restrict__ row_topk, float* __restrict__ row_weight,
+    int* __restrict__ err) {
     extern __shared__ int s_mem[];
-    __shared__ int s_chunk, s_last;
-    // 1. counts
-    while (true) {
-        if (threadIdx.x == 0) s_chunk = atomicAdd(&sync[0], 1);
-        __syncthreads();
-        const int c = s_chunk;
-        __syncthreads();
-        if (c >= chunks) break;
-        count_chunk(topk_idx, n_entries, E, c, hist, err, s_mem);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();  // this chunk's histogram before the count of finished chunks
-            s_last = atomicAdd(&sync[2], 1) == chunks - 1;
-        }
-        __syncthreads();
-        if (s_last) {
-            // 2. the last chunk is in: every histogram is visible
-            __threadfence();
-            scan_body(hist, chunks, E, count, off, poff, chunk_base, block_expert, block_rows, n_blocks, max_count,
-                      row_token, row_topk, row_weight);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x / 32;
+    int* s_next = s_mem;                       // [E] histogram (phase 1), next free slot (phase 3)
+    int* s_wcnt = s_mem + E;                   // [nwarps][E]
+    int* s_part = s_mem + E * (1 + nwarps);    // [2 * blockDim.x]
+    int* s_tot = s_part + 2 * blockDim.x;      // [E] count of each expert
+    int* s_base = s_tot + E;                   // [E] base of the current slot chunk
+    int* s_poff = s_base + E;                  // [E] padded offset of each expert
+    __shared__ __align__(8) int s_warp2[64];
+    __shared__ int s_chunk, s_ok, s_max;
+    // Every chunk has a CTA of its own when chunks <= gridDim.x: each CTA then
+    // takes one chunk (or none), counts it, and later slots the same chunk
+    // from the ids and weights it kept in registers.
+    const bool one_pass = chunks <= static_cast<int>(gridDim.x);
+    int e_r[kFusedPer];
+    float w_r[kFusedPer];
+    int c = chunks;
+    if (tid == 0) {
+        s_max = 0;
+        s_chunk = atomicAdd(&sync[0], 1);
+    }
+    for (int e = tid; e < E; e += blockDim.x) s_next[e] = 0;
+    __syncthreads();
+    if (one_pass) {
+        c = s_chunk;
+        if (c < chunks) {
+            const int64_t base = static_cast<int64_t>(c) * kRouteChunk;
+            const int64_t end = min(base + kRouteChunk, n_entries);
+            bool bad = false;
+#pragma unroll
+            for (int q = 0; q < kFusedPer; ++q) {
+                const int64_t i = base + q * kScanThreads + tid;
+                e_r[q] = entry_expert(topk_idx, i, end, E, &bad);
+                w_r[q] = i < end ? __ldg(topk_w + i) : 0.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < kFusedPer; ++q) {
+                const uint32_t same = __match_any_sync(0xffffffffu, e_r[q]);
+                if (e_r[q] >= 0 && lane == __ffs(same) - 1) atomicAdd(&s_next[e_r[q]], __popc(same));
+            }
+            if (bad) atomicOr(err, kDevErrBadExpert);
             __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomicExch(&sync[3], 1);
+            for (int e = tid; e < E; e += blockDim.x) hist[static_cast<size_t>(c) * E + e] = s_next[e];
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();  // this chunk's histogram row before the count of finished chunks
+                atomicAdd(&sync[2], 1);
             }
         }
+    } else {
+        // 1. counts, chunks taken from the counter until none is left
+        while (true) {
+            const int cc = s_chunk;
+            __syncthreads();
+            if (cc >= chunks) break;
+            count_chunk(topk_idx, n_entries, E, cc, hist, err, s_mem);
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();
+                atomicAdd(&sync[2], 1);
+                s_chunk = atomicAdd(&sync[0], 1);
+            }
+            __syncthreads();
+        }
     }
-    // 3. stable slots, once the scans are released
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         const uint64_t deadline = globaltimer_ns() + kRouteWaitNs;
         bool ok = true;
-        while (ld_acquire_gpu_int(&sync[3]) == 0) {
+        while (ld_acquire_gpu_int(&sync[2]) < chunks) {
             if (globaltimer_ns() > deadline) {
                 ok = false;
                 break;
             }
-            __nanosleep(256);
+            __nanosleep(128);
         }
         if (!ok) {
             atomicOr(err, kDevErrTimeout);
             atomicCAS(err + 1, 0, 1 + 99);
         }
-        s_last = ok;
+        s_ok = ok;
+        if (!one_pass) s_chunk = atomicAdd(&sync[1], 1);  // first slot chunk of this CTA
     }
     __syncthreads();
-    if (!s_last) return;
-    while (true) {
-        if (threadIdx.x == 0) s_chunk = atomicAdd(&sync[1], 1);
+    if (!s_ok) return;
+    if (!one_pass) c = s_chunk;
+    // 2. totals and this CTA's chunk base, then the scans, in every CTA
+    chunk_sums(hist, chunks, E, min(c, chunks), s_part, s_tot, s_base);
+    const int c_e = tid < E ? s_tot[tid] : 0;
+    const int padded = (c_e + kBlockM - 1) / kBlockM * kBlockM;
+    int inc_c, inc_p;
+    block_inclusive_scan2(c_e, padded, s_warp2, inc_c, inc_p);
+    if (tid < E) {
+        s_poff[tid] = inc_p - padded;
+        if (blockIdx.x == 0) {
+            count[tid] = c_e;
+            off[tid] = inc_c - c_e;
+            poff[tid] = inc_p - padded;
+            if (c_e > 0) atomicMax(&s_max, c_e);
+            if (tid == E - 1) {
+                off[E] = inc_c;
+                poff[E] = inc_p;
+                *n_blocks = inc_p / kBlockM;
+            }
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && tid == 0) *max_count = s_max;
+    // the row-block tables and the padding rows: one expert per warp of the grid
+    for (int x = blockIdx.x * nwarps + warp; x < E; x += gridDim.x * nwarps) {
+        const int c_x = s_tot[x], p_x = s_poff[x];
+        const int nb = (c_x + kBlockM - 1) / kBlockM;
+        for (int b = lane; b < nb; b += 32) {
+            block_expert[p_x / kBlockM + b] = x;
+            block_rows[p_x / kBlockM + b] = min(kBlockM, c_x - b * kBlockM);
+        }
+        for (int r = p_x + c_x + lane; r < p_x + nb * kBlockM; r += 32) {
+            row_token[r] = -1;
+            row_topk[r] = -1;
+            row_weight[r] = 0.0f;
+        }
+    }
+    // 3. stable slots
+    while (c < chunks) {
+        for (int e = tid; e < E; e += blockDim.x) {
+            s_next[e] = s_poff[e] + s_base[e];
+            for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
+        }
         __syncthreads();
-        const int c = s_chunk;
+        if (one_pass) {
+            const int64_t base = static_cast<int64_t>(c) * kRouteChunk;
+            const int64_t end = min(base + kRouteChunk, n_entries);
+#pragma unroll
+            for (int q = 0; q < kFusedPer; ++q) {
+                const int64_t i = base + q * kScanThreads + tid;
+                const int slot = rank_round(e_r[q], E, s_next, s_wcnt);
+                if (i < end) write_slot(i, slot, w_r[q], k, slot_of, row_token, row_topk, row_weight);
+            }
+            break;
+        }
+        slot_rank(topk_idx, topk_w, n_entries, k, E, c, s_next, s_wcnt, slot_of, row_token, row_topk, row_weight);
+        if (tid == 0) s_chunk = atomicAdd(&sync[1], 1);
         __syncthreads();
-        if (c >= chunks) break;
-        slot_chunk(topk_idx, topk_w, n_entries, k, E, c, poff, chunk_base, slot_of, row_token, row_topk, row_weight,
-                   s_mem);
-        __syncthreads();
+        c = s_chunk;
+        if (c < chunks) chunk_sums(hist, chunks, E, c, s_part, s_tot, s_base);
     }
 }
 
@@ -486,7 +668,21 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
     int* off = reinterpret_cast<int*>(ws + L.off);
     int* poff = reinterpret_cast<int*>(ws + L.poff);
     int* chunk_base = reinterpret_cast<int*>(ws + L.chunk_base);
-    if (L.chunks == 1) {  // one kernel for a decode-sized batch
+    if (L.E <= kFusedMaxExperts) {  // the whole plan in one launch
+        // the error record and the plan's four scheduling words start at zero
+        cudaError_t st = cudaMemsetAsync(err, 0, kErrWords * sizeof(int), s);
+        if (st != cudaSuccess) return st;
+        const int ctas = std::min(std::max(L.chunks, kFusedMinCtas), 512);
+        const size_t smem = (static_cast<size_t>(L.E) * (4 + kScanThreads / 32) + 2 * kScanThreads) * sizeof(int);
+        route_fused_kernel<<<ctas, kScanThreads, smem, s>>>(
+            topk_idx, topk_w, n, L.k, L.E, L.chunks, err + kErrSyncOff, hist, count, off, poff,
+            reinterpret_cast<int*>(ws + L.block_expert), reinterpret_cast<int*>(ws + L.block_rows),
+            reinterpret_cast<int*>(ws + L.n_blocks), reinterpret_cast<int*>(ws + L.max_count),
+            reinterpret_cast<int*>(ws + L.slot_of), reinterpret_cast<int*>(ws + L.row_token),
+            reinterpret_cast<int*>(ws + L.row_topk), reinterpret_cast<float*>(ws + L.row_weight), err);
+        return cudaGetLastError();
+    }
+    if (L.chunks == 1) {  // one kernel for a decode-sized batch of many experts
         const int threads = small_threads(L.E);
         const size_t smem = static_cast<size_t>(L.E) * (3 + threads / 32) * sizeof(int);
         route_small_kernel<<<1, threads, smem, s>>>(
@@ -497,19 +693,8 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
             reinterpret_cast<int*>(ws + L.row_topk), reinterpret_cast<float*>(ws + L.row_weight), err);
         return cudaGetLastError();
     }
-    // the error record and the fused plan's four scheduling words start at zero
     cudaError_t st = cudaMemsetAsync(err, 0, kErrWords * sizeof(int), s);
     if (st != cudaSuccess) return st;
-    if (L.E <= kFusedMaxExperts && L.chunks > 0) {  // the whole plan in one launch
-        const size_t smem = static_cast<size_t>(L.E) * (1 + kScanThreads / 32) * sizeof(int);
-        route_fused_kernel<<<std::min(L.chunks, 512), kScanThreads, smem, s>>>(
-            topk_idx, topk_w, n, L.k, L.E, L.chunks, err + kErrSyncOff, hist, count, off, poff, chunk_base,
-            reinterpret_cast<int*>(ws + L.block_expert), reinterpret_cast<int*>(ws + L.block_rows),
-            reinterpret_cast<int*>(ws + L.n_blocks), reinterpret_cast<int*>(ws + L.max_count),
-            reinterpret_cast<int*>(ws + L.slot_of), reinterpret_cast<int*>(ws + L.row_token),
-            reinterpret_cast<int*>(ws + L.row_topk), reinterpret_cast<float*>(ws + L.row_weight), err);
-        return cudaGetLastError();
-    }
     if (L.chunks > 0) {
         route_count_kernel<<<L.chunks, kCountThreads, L.E * sizeof(int), s>>>(topk_idx, n, L.E, hist, err);
         if ((st = cudaGetLastError()) != cudaSuccess) return st;
