@@ -349,7 +349,8 @@ def roofline(L, stage_ms, pk, mma):
              peak_note=f"FP8 = 2 x {pk['source']} burst bf16 cuBLAS rate ({pk['bf16']} TF/s), the nominal FP8/bf16 "
                        f"ratio of the dense tensor rates")
     if mma:
-        r.update(frac_vs_mma=ach / mma["tflops"], mma_ceiling_tflops=mma["tflops"])
+        r.update(frac_vs_mma=ach / mma["tflops"], mma_ceiling_tflops=mma["tflops"],
+                 frac_vs_stream=ach / mma["stream"]["tflops"], stream_ceiling_tflops=mma["stream"]["tflops"])
     return r
 
 
@@ -377,13 +378,23 @@ def gather_leg(L, args, world, flush, dev):
                      "128-row stage) instead of one 128-row box of the expert-major pool")
 
 
-def mma_ceiling(moe):
+def mma_ceiling(moe, dev):
     """The block-scaled MMA (the GEMMs' instruction) issued back to back on every
-    SM from fixed shared-memory operands: the tensor pipe's rate on this GPU."""
+    SM from fixed shared-memory operands: the tensor pipe's rate on this GPU.
+    Beside it, the same MMAs fed by the layer-1 tile's own operand stream (TMA
+    ring, scale copies, no epilogue) from L2-resident operands, with the SM
+    clocks sampled while it runs: what this tile shape can reach with its
+    operands moving, under the board's power limit."""
     tflops, ctas, ms = moe.selftest_mma_rate(kblocks=16384, repeats=3)
+    with ClockSampler(dev.index) as clk:
+        s_tf, s_ctas, s_ms = moe.selftest_stream_rate(kblocks=16384, repeats=20)
     return dict(tflops=tflops, ctas=ctas, ms=ms,
                 note="moe_selftest_mma_rate: M=128 N=256 K=32 kind::mxf8f6f4 block-scaled MMAs, one CTA per SM, "
-                     "16384 x 4 per CTA, best of 3 launches")
+                     "16384 x 4 per CTA, best of 3 launches",
+                stream=dict(tflops=s_tf, ctas=s_ctas, ms=s_ms, clocks=clk.summary(),
+                            note="moe_selftest_stream_rate: the same MMAs fed by the layer-1 tile's 4-stage TMA ring "
+                                 "(128-row E4M3 A box, 256-row E2M1 B box, scale copies), no epilogue, one CTA per "
+                                 "SM, 16384 k-blocks per CTA, best of 20 launches"))
 
 
 def decode_leg(moe, args, world, flush, dev, pk):
@@ -540,7 +551,7 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     pk = peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    mma = mma_ceiling(moe)
+    mma = mma_ceiling(moe, dev)
     L = Layer(moe, w, dev)
     t_max, stage_ms, clk = timed_steps(L, args, world, flush, dev)
     value = world * L.flops * args.steps / t_max / 1e12

@@ -320,6 +320,31 @@ int moe_selftest_bounded_wait(int arrive, uint64_t timeout_ns, int32_t* out, voi
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED (not sm_103), MOE_ERR_CUDA. */
 int moe_selftest_mma_rate(int kblocks, int32_t* status, int* ctas, void* stream);
 
+/* Operand-stream ceiling of the layer-1 GEMM tile (no counterpart on the
+ * pages; a second calibration for the roofline of the GEMMs).  The MMAs of
+ * moe_selftest_mma_rate, fed as the expert kernel feeds them: one CTA per SM,
+ * a 4-stage ring of 50 KB stages filled by TMA (a 128-row E4M3 box of A, the
+ * 256-row two-plane E2M1 box of B expanded to one byte per element, the A
+ * scale chunk and the B scale pair), a thread copying each stage's scales
+ * into tensor memory and the MMA thread; no epilogue.  CTA c reads row block
+ * (c / 16) % 16 of A and weight rows 128 * (c % 16) .. +128 of both planes of
+ * B, cycling through the 56 k-blocks of K = 7168.  The values only need to be
+ * finite codes; the product is discarded.
+ *   a        device E4M3 codes [2048][7168] (row-major, 16-byte aligned)
+ *   b        device E2M1 codes [2][2048][7168/2] (two per byte, 16-byte aligned)
+ *   sfa      device UE8M0 scale chunks [16][56][512] (tensor-core layout)
+ *   sfb      device UE8M0 scale chunk pairs [16][56][1024]
+ *   kblocks  k-blocks per CTA, 1 .. 2^20; the work is ctas * kblocks *
+ *            2*128*256*128 FLOP
+ *   status   device int32, written: MOE_OK, or MOE_ERR_TIMEOUT if a stage
+ *            wait gave up after 2 s of global time (the kernel then returns)
+ *   ctas     out (host): the number of CTAs launched (the SM count)
+ * Errors: MOE_ERR_INVALID_ARG (null or unaligned pointers, kblocks out of
+ * range), MOE_ERR_UNSUPPORTED (not sm_103), MOE_ERR_CUDA.  The caller owns
+ * every buffer and times the launch on `stream`. */
+int moe_selftest_stream_rate(const void* a, const void* b, const void* sfa, const void* sfb, int kblocks,
+                             int32_t* status, int* ctas, void* stream);
+
 /* Failure-detection self-test of moe_expert_fused (no counterpart on the
  * pages): runs the fused launch with its readiness counters set so that no
  * row block ever becomes ready, so every layer-2 tile's bounded wait expires

@@ -49,7 +49,7 @@ _EXPORT_DTYPE = dict(count=torch.int32, off=torch.int32, poff=torch.int32, slot_
 SYMBOLS = ("moe_plan_workspace_bytes", "moe_weight_scales_bytes", "moe_prepare_weight_scales", "moe_plan",
            "moe_dispatch", "moe_expert_l1", "moe_expert_l2", "moe_combine", "moe_forward", "moe_plan_check",
            "moe_plan_export", "moe_error_string", "moe_expert_offsets_static", "moe_selftest_bounded_wait",
-           "moe_selftest_mma_rate", "moe_expert_fused", "moe_selftest_fused_wait")
+           "moe_selftest_mma_rate", "moe_expert_fused", "moe_selftest_fused_wait", "moe_selftest_stream_rate")
 
 
 class MoeError(RuntimeError):
@@ -140,6 +140,8 @@ def lib():
             L.moe_selftest_bounded_wait.argtypes = [i32, ctypes.c_uint64, P, P]
             L.moe_selftest_mma_rate.restype = i32
             L.moe_selftest_mma_rate.argtypes = [i32, P, ctypes.POINTER(i32), P]
+            L.moe_selftest_stream_rate.restype = i32
+            L.moe_selftest_stream_rate.argtypes = [P, P, P, P, i32, P, ctypes.POINTER(i32), P]
             L.moe_error_string.restype = ctypes.c_char_p
             L.moe_error_string.argtypes = [i32]
             _lib = L
@@ -337,6 +339,38 @@ def selftest_mma_rate(kblocks: int = 16384, repeats: int = 3, stream=None):
         _check(int(status.item()), "moe_selftest_mma_rate (device)")
         if i > 0:
             ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+    tflops = ctas.value * kblocks * MMA_FLOP_PER_KBLOCK / (best / 1e3) / 1e12
+    return tflops, ctas.value, best
+
+
+def selftest_stream_rate(kblocks: int = 8192, repeats: int = 3, stream=None):
+    """moe_selftest_stream_rate timed with CUDA events on synthetic operands
+    (finite E4M3 codes, random E2M1 codes, unit scales): the best of `repeats`
+    launches (after one warm-up), as (TFLOP/s, CTAs, ms per launch)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    # E4M3 codes with bit 3 clear: never 0x7F / 0xFF (NaN)
+    a = (torch.randint(0, 256, (2048 * 7168,), dtype=torch.int32, device=dev, generator=g) & 0xF7).to(torch.uint8)
+    b = torch.randint(0, 256, (2 * 2048 * 3584,), dtype=torch.int32, device=dev, generator=g).to(torch.uint8)
+    sfa = torch.full((16 * 56 * 512,), 127, dtype=torch.uint8, device=dev)
+    sfb = torch.full((16 * 56 * 1024,), 127, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream() if stream is None else stream
+    ctas = ctypes.c_int(0)
+    best = None
+    for i in range(repeats + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        _check(lib().moe_selftest_stream_rate(_ptr(a), _ptr(b), _ptr(sfa), _ptr(sfb), int(kblocks), _ptr(status),
+                                              ctypes.byref(ctas), ctypes.c_void_p(s.cuda_stream)),
+               "moe_selftest_stream_rate")
+        e1.record(s)
+        e1.synchronize()
+        _check(int(status.item()), "moe_selftest_stream_rate (device)")
+        if i > 0:
+            ms = e0.elapsed_time(e1)
             best = ms if best is None else min(best, ms)
     tflops = ctas.value * kblocks * MMA_FLOP_PER_KBLOCK / (best / 1e3) / 1e12
     return tflops, ctas.value, best

@@ -367,6 +367,18 @@ int moe_selftest_mma_rate(int kblocks, int32_t* status, int* ctas, void* stream)
     return cuda_status(launch_mma_rate_selftest(kblocks, sms, status, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_selftest_stream_rate(const void* a, const void* b, const void* sfa, const void* sfb, int kblocks,
+                             int32_t* status, int* ctas, void* stream) {
+    if (!a || !b || !sfa || !sfb || !status || !ctas || kblocks < 1 || kblocks > (1 << 20)) return MOE_ERR_INVALID_ARG;
+    for (const void* p : {a, b, sfa, sfb})
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = device_info(&sms);
+    if (rc) return rc;
+    *ctas = sms;
+    return cuda_status(launch_stream_rate_selftest(a, b, sfa, sfb, kblocks, sms, status, static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_error_string(int status) {
     switch (status) {
         case MOE_OK: return "ok";

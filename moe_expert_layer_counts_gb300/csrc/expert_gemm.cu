@@ -884,6 +884,12 @@ bool make_out_map(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows) {
 
 }  // namespace
 
+bool make_layer1_operand_maps(CUtensorMap* a_map, const void* a, CUtensorMap* b_map, const void* b, uint64_t K,
+                              uint64_t rows) {
+    return make_map(a_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, a, K, rows, K, kBlockM) &&
+           make_map_3d_fp4(b_map, b, K, rows, 2);
+}
+
 namespace {
 
 // Opt a kernel into its dynamic shared memory once per device.

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/moe.h"
@@ -66,6 +67,13 @@ cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves
 
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t timeout_ns, int32_t* out, cudaStream_t s);
 cudaError_t launch_mma_rate_selftest(int kblocks, int ctas, int32_t* status, cudaStream_t s);
+cudaError_t launch_stream_rate_selftest(const void* a, const void* b, const void* sfa, const void* sfb, int kblocks,
+                                        int ctas, int32_t* status, cudaStream_t s);
+// The layer-1 GEMM's operand maps: A as 128-row boxes of a [rows, K] E4M3
+// matrix, B as the 3-D two-plane E2M1 map [2][rows][K] (256 weight rows per
+// request), both as the expert kernel builds them.
+bool make_layer1_operand_maps(CUtensorMap* a_map, const void* a, CUtensorMap* b_map, const void* b, uint64_t K,
+                              uint64_t rows);
 
 struct GemmLaunch {
     const void* w_q;      // packed e2m1 weights [E, N, K/2]

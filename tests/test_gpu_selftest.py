@@ -42,3 +42,15 @@ def test_mma_rate_calibration(moe):
     assert 1000.0 < tflops < 20000.0, tflops
     with pytest.raises(moe.MoeError):
         moe.selftest_mma_rate(kblocks=0)
+
+
+def test_stream_rate_calibration(moe):
+    """The operand-stream ceiling kernel (the GEMM tile's TMA ring, scale
+    copies and MMAs, no epilogue) completes with status OK on every SM, at a
+    rate no higher than the bare MMA ceiling allows."""
+    mma, _, _ = moe.selftest_mma_rate(kblocks=2048, repeats=1)
+    tflops, ctas, ms = moe.selftest_stream_rate(kblocks=1024, repeats=1)
+    assert ctas >= 100
+    assert 500.0 < tflops < 1.1 * mma, (tflops, mma)
+    with pytest.raises(moe.MoeError):
+        moe.selftest_stream_rate(kblocks=0)
