@@ -300,19 +300,24 @@ __global__ void __launch_bounds__(kSmallMaxThreads) route_slot_kernel(
 
 // The whole plan in ONE multi-CTA launch, for at most kFusedMaxExperts
 // experts and any number of entries:
-//   1. histograms of chunks, each chunk taken from a work counter (sync[0]);
-//      a finished chunk is counted in sync[2] (release);
-//   2. once sync[2] reaches the number of chunks (acquire), EVERY CTA sums the
-//      histogram rows itself (the per-expert totals, and the base of the slot
-//      chunk it takes next from sync[1]) and scans the totals, so no CTA waits
-//      for another's scan; CTA 0 writes the count / offset tables, and the
+//   1. every CTA takes a chunk number from a counter (sync[0]) and counts that
+//      chunk, keeping its ids and weights in registers; a counted chunk is
+//      added to sync[2] (release).  A CTA then waits until sync[2] reaches the
+//      number of chunks (acquire), and while it waits it takes any chunk still
+//      untaken from the same counter and counts it from memory (sync[3]
+//      counts those) -- a chunk is taken only by a running CTA and a waiting
+//      CTA keeps taking chunks, so every chunk is counted whether or not all
+//      CTAs are resident;
+//   2. EVERY CTA sums the histogram rows itself (the per-expert totals and the
+//      base of its own chunk) and scans the totals, so no CTA waits for
+//      another's scan; CTA 0 writes the count / offset tables, and the
 //      row-block tables and padding rows are shared out one expert per warp
 //      over the whole grid;
-//   3. stable slots of the chunks taken from sync[1], as route_slot.
-// A CTA waits only once no chunk of phase 1 is left to take, so every chunk
-// of phase 1 is held by a running CTA: no co-residency is needed.  The wait
-// is bounded (1 s of global time; the error record gets MOE_ERR_TIMEOUT).
-// sync[0..3] must be zero at launch.
+//   3. every CTA ranks the chunk it holds in registers; chunks counted from
+//      memory (marked in chunk_kind) are ranked from memory, taken from a
+//      second counter (sync[1]).
+// The wait is bounded (1 s of global time; the error record gets
+// MOE_ERR_TIMEOUT).  sync[0..3] must be zero at launch.
 constexpr int kFusedMaxExperts = 256;
 constexpr int kFusedMinCtas = 16;  // CTAs that share the tables and padding rows of a small batch
 constexpr uint64_t kRouteWaitNs = 1000000000ull;
@@ -383,11 +388,11 @@ static_assert(kFusedPer * kScanThreads == kRouteChunk, "a chunk is whole rounds 
 
 __global__ void __launch_bounds__(kScanThreads) route_fused_kernel(
     const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int64_t n_entries, int k, int E,
-    int chunks, int* __restrict__ sync, int* __restrict__ hist, int* __restrict__ count, int* __restrict__ off,
-    int* __restrict__ poff, int* __restrict__ block_expert, int* __restrict__ block_rows,
-    int* __restrict__ n_blocks, int* __restrict__ max_count, int* __restrict__ slot_of,
-    int* __restrict__ row_token, int* __restrict__ row_topk, float* __restrict__ row_weight,
-    int* __restrict__ err) {
+    int chunks, int* __restrict__ sync, int* __restrict__ hist, int* __restrict__ chunk_kind,
+    int* __restrict__ count, int* __restrict__ off, int* __restrict__ poff, int* __restrict__ block_expert,
+    int* __restrict__ block_rows, int* __restrict__ n_blocks, int* __restrict__ max_count,
+    int* __restrict__ slot_of, int* __restrict__ row_token, int* __restrict__ row_topk,
+    float* __restrict__ row_weight, int* __restrict__ err) {
     extern __shared__ int s_mem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x / 32;
     int* s_next = s_mem;                       // [E] histogram (phase 1), next free slot (phase 3)
@@ -397,84 +402,84 @@ __global__ void __launch_bounds__(kScanThreads) route_fused_kernel(
     int* s_base = s_tot + E;                   // [E] base of the current slot chunk
     int* s_poff = s_base + E;                  // [E] padded offset of each expert
     __shared__ __align__(8) int s_warp2[64];
-    __shared__ int s_chunk, s_ok, s_max;
-    // Every chunk has a CTA of its own when chunks <= gridDim.x: each CTA then
-    // takes one chunk (or none), counts it, and later slots the same chunk
-    // from the ids and weights it kept in registers.
-    const bool one_pass = chunks <= static_cast<int>(gridDim.x);
+    __shared__ int s_chunk, s_state, s_max;
+    constexpr int kDone = -1, kWait = -2, kTimedOut = -3;
     int e_r[kFusedPer];
     float w_r[kFusedPer];
-    int c = chunks;
     if (tid == 0) {
         s_max = 0;
         s_chunk = atomicAdd(&sync[0], 1);
     }
     for (int e = tid; e < E; e += blockDim.x) s_next[e] = 0;
     __syncthreads();
-    if (one_pass) {
-        c = s_chunk;
-        if (c < chunks) {
-            const int64_t base = static_cast<int64_t>(c) * kRouteChunk;
-            const int64_t end = min(base + kRouteChunk, n_entries);
-            bool bad = false;
+    // 1. the chunk this CTA holds in registers
+    const int c0 = s_chunk;
+    if (c0 < chunks) {
+        const int64_t base = static_cast<int64_t>(c0) * kRouteChunk;
+        const int64_t end = min(base + kRouteChunk, n_entries);
+        bool bad = false;
 #pragma unroll
-            for (int q = 0; q < kFusedPer; ++q) {
-                const int64_t i = base + q * kScanThreads + tid;
-                e_r[q] = entry_expert(topk_idx, i, end, E, &bad);
-                w_r[q] = i < end ? __ldg(topk_w + i) : 0.0f;
-            }
-#pragma unroll
-            for (int q = 0; q < kFusedPer; ++q) {
-                const uint32_t same = __match_any_sync(0xffffffffu, e_r[q]);
-                if (e_r[q] >= 0 && lane == __ffs(same) - 1) atomicAdd(&s_next[e_r[q]], __popc(same));
-            }
-            if (bad) atomicOr(err, kDevErrBadExpert);
-            __syncthreads();
-            for (int e = tid; e < E; e += blockDim.x) hist[static_cast<size_t>(c) * E + e] = s_next[e];
-            __syncthreads();
-            if (tid == 0) {
-                __threadfence();  // this chunk's histogram row before the count of finished chunks
-                atomicAdd(&sync[2], 1);
-            }
+        for (int q = 0; q < kFusedPer; ++q) {
+            const int64_t i = base + q * kScanThreads + tid;
+            e_r[q] = entry_expert(topk_idx, i, end, E, &bad);
+            w_r[q] = i < end ? __ldg(topk_w + i) : 0.0f;
         }
-    } else {
-        // 1. counts, chunks taken from the counter until none is left
-        while (true) {
-            const int cc = s_chunk;
-            __syncthreads();
-            if (cc >= chunks) break;
-            count_chunk(topk_idx, n_entries, E, cc, hist, err, s_mem);
+#pragma unroll
+        for (int q = 0; q < kFusedPer; ++q) {
+            const uint32_t same = __match_any_sync(0xffffffffu, e_r[q]);
+            if (e_r[q] >= 0 && lane == __ffs(same) - 1) atomicAdd(&s_next[e_r[q]], __popc(same));
+        }
+        if (bad) atomicOr(err, kDevErrBadExpert);
+        __syncthreads();
+        for (int e = tid; e < E; e += blockDim.x) hist[static_cast<size_t>(c0) * E + e] = s_next[e];
+        __syncthreads();
+        if (tid == 0) {
+            chunk_kind[c0] = 1;  // ranked from registers by this CTA
+            __threadfence();     // the histogram row and the mark before the count of finished chunks
+            atomicAdd(&sync[2], 1);
+        }
+    }
+    // wait until every chunk is counted, counting untaken chunks meanwhile
+    const uint64_t deadline = globaltimer_ns() + kRouteWaitNs;
+    while (true) {
+        if (tid == 0) {
+            int state = kWait;
+            if (ld_acquire_gpu_int(&sync[2]) >= chunks) {
+                state = kDone;
+            } else if (*reinterpret_cast<volatile int*>(&sync[0]) < chunks) {
+                const int c = atomicAdd(&sync[0], 1);
+                if (c < chunks) state = c;
+            } else if (globaltimer_ns() > deadline) {
+                state = kTimedOut;
+            } else {
+                __nanosleep(128);
+            }
+            s_state = state;
+        }
+        __syncthreads();
+        const int state = s_state;
+        __syncthreads();
+        if (state == kDone) break;
+        if (state == kTimedOut) {
+            if (tid == 0) {
+                atomicOr(err, kDevErrTimeout);
+                atomicCAS(err + 1, 0, 1 + 99);
+            }
+            return;
+        }
+        if (state >= 0) {
+            count_chunk(topk_idx, n_entries, E, state, hist, err, s_mem);
             __syncthreads();
             if (tid == 0) {
+                chunk_kind[state] = 2;  // ranked from memory in phase 3
+                atomicAdd(&sync[3], 1);
                 __threadfence();
                 atomicAdd(&sync[2], 1);
-                s_chunk = atomicAdd(&sync[0], 1);
             }
-            __syncthreads();
         }
     }
-    if (tid == 0) {
-        const uint64_t deadline = globaltimer_ns() + kRouteWaitNs;
-        bool ok = true;
-        while (ld_acquire_gpu_int(&sync[2]) < chunks) {
-            if (globaltimer_ns() > deadline) {
-                ok = false;
-                break;
-            }
-            __nanosleep(128);
-        }
-        if (!ok) {
-            atomicOr(err, kDevErrTimeout);
-            atomicCAS(err + 1, 0, 1 + 99);
-        }
-        s_ok = ok;
-        if (!one_pass) s_chunk = atomicAdd(&sync[1], 1);  // first slot chunk of this CTA
-    }
-    __syncthreads();
-    if (!s_ok) return;
-    if (!one_pass) c = s_chunk;
     // 2. totals and this CTA's chunk base, then the scans, in every CTA
-    chunk_sums(hist, chunks, E, min(c, chunks), s_part, s_tot, s_base);
+    chunk_sums(hist, chunks, E, min(c0, chunks), s_part, s_tot, s_base);
     const int c_e = tid < E ? s_tot[tid] : 0;
     const int padded = (c_e + kBlockM - 1) / kBlockM * kBlockM;
     int inc_c, inc_p;
@@ -509,29 +514,41 @@ __global__ void __launch_bounds__(kScanThreads) route_fused_kernel(
             row_weight[r] = 0.0f;
         }
     }
-    // 3. stable slots
-    while (c < chunks) {
+    // 3. stable slots: the chunk held in registers
+    if (c0 < chunks) {
         for (int e = tid; e < E; e += blockDim.x) {
             s_next[e] = s_poff[e] + s_base[e];
             for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
         }
         __syncthreads();
-        if (one_pass) {
-            const int64_t base = static_cast<int64_t>(c) * kRouteChunk;
-            const int64_t end = min(base + kRouteChunk, n_entries);
+        const int64_t base = static_cast<int64_t>(c0) * kRouteChunk;
+        const int64_t end = min(base + kRouteChunk, n_entries);
 #pragma unroll
-            for (int q = 0; q < kFusedPer; ++q) {
-                const int64_t i = base + q * kScanThreads + tid;
-                const int slot = rank_round(e_r[q], E, s_next, s_wcnt);
-                if (i < end) write_slot(i, slot, w_r[q], k, slot_of, row_token, row_topk, row_weight);
-            }
-            break;
+        for (int q = 0; q < kFusedPer; ++q) {
+            const int64_t i = base + q * kScanThreads + tid;
+            const int slot = rank_round(e_r[q], E, s_next, s_wcnt);
+            if (i < end) write_slot(i, slot, w_r[q], k, slot_of, row_token, row_topk, row_weight);
         }
-        slot_rank(topk_idx, topk_w, n_entries, k, E, c, s_next, s_wcnt, slot_of, row_token, row_topk, row_weight);
-        if (tid == 0) s_chunk = atomicAdd(&sync[1], 1);
+    }
+    // then the chunks counted from memory (final: counted before sync[2] was)
+    if (__ldcg(&sync[3]) == 0) return;
+    while (true) {
         __syncthreads();
-        c = s_chunk;
-        if (c < chunks) chunk_sums(hist, chunks, E, c, s_part, s_tot, s_base);
+        if (tid == 0) {
+            int c = atomicAdd(&sync[1], 1);
+            while (c < chunks && __ldcg(&chunk_kind[c]) != 2) c = atomicAdd(&sync[1], 1);
+            s_chunk = c;
+        }
+        __syncthreads();
+        const int c = s_chunk;
+        if (c >= chunks) break;
+        chunk_sums(hist, chunks, E, c, s_part, s_tot, s_base);
+        for (int e = tid; e < E; e += blockDim.x) {
+            s_next[e] = s_poff[e] + s_base[e];
+            for (int w = 0; w < nwarps; ++w) s_wcnt[w * E + e] = 0;
+        }
+        __syncthreads();
+        slot_rank(topk_idx, topk_w, n_entries, k, E, c, s_next, s_wcnt, slot_of, row_token, row_topk, row_weight);
     }
 }
 
@@ -675,7 +692,7 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
         const int ctas = std::min(std::max(L.chunks, kFusedMinCtas), 512);
         const size_t smem = (static_cast<size_t>(L.E) * (4 + kScanThreads / 32) + 2 * kScanThreads) * sizeof(int);
         route_fused_kernel<<<ctas, kScanThreads, smem, s>>>(
-            topk_idx, topk_w, n, L.k, L.E, L.chunks, err + kErrSyncOff, hist, count, off, poff,
+            topk_idx, topk_w, n, L.k, L.E, L.chunks, err + kErrSyncOff, hist, chunk_base, count, off, poff,
             reinterpret_cast<int*>(ws + L.block_expert), reinterpret_cast<int*>(ws + L.block_rows),
             reinterpret_cast<int*>(ws + L.n_blocks), reinterpret_cast<int*>(ws + L.max_count),
             reinterpret_cast<int*>(ws + L.slot_of), reinterpret_cast<int*>(ws + L.row_token),

@@ -1,5 +1,8 @@
-"""GPU dispatch plan (route_count / route_scan / route_slot) against the
-oracle plan, bit-exact, on every workload and on edge cases."""
+"""GPU dispatch plan against the oracle plan, bit-exact, on every workload and
+on edge cases: the one-launch plan (route_fused, E <= 256: one chunk per CTA,
+or several when the chunks outnumber its 512 CTAs), the one-CTA plan for more
+experts and at most 2048 entries (route_small), and the chunked count / scan /
+slot kernels beyond."""
 import numpy as np
 import pytest
 import torch
@@ -69,15 +72,28 @@ def test_plan_edge_cases(moe, oracle):
 @pytest.mark.parametrize("n", [1, 2047, 2048, 2049, 4096])
 @pytest.mark.parametrize("E", [8, 300, 512, 1024])
 def test_plan_one_kernel_and_chunked_paths(moe, oracle, n, E):
-    """Up to 2048 entries the plan is one single-CTA kernel, above it the
-    chunked count / scan / slot kernels: both sides of the switch, with
-    skipped and bad ids; the expert counts give the routing kernels 1024,
-    1024, 640 and 256 threads."""
+    """Both sides of the 2048-entry switch, with skipped and bad ids: E = 8
+    runs the one-launch plan on either side (one chunk on 16 CTAs, or two);
+    more experts run the one-CTA kernel up to 2048 entries and the chunked
+    count / scan / slot kernels above it, with 1024, 640 and 256 threads."""
     rng = np.random.default_rng(n + E)
     idx = rng.integers(-1, E, size=(n, 1))
     if n > 3:
         idx[n // 2, 0] = E
     compare_plan(moe, oracle, idx, rng.random((n, 1)), E)
+
+
+@pytest.mark.parametrize("n", [512 * 2048, 512 * 2048 + 1, 1_100_000])
+def test_plan_more_chunks_than_ctas(moe, oracle, n):
+    """The one-launch plan has at most 512 CTAs: at 512 chunks each still
+    counts and slots one chunk from registers; beyond it the CTAs take
+    further chunks from the work counters."""
+    rng = np.random.default_rng(n)
+    E = 64
+    # skewed ids: a few hot experts, every expert present, some skipped entries
+    idx = np.minimum(rng.zipf(1.3, size=n) - 1, E - 1)
+    idx[rng.random(n) < 0.05] = -1
+    compare_plan(moe, oracle, idx.reshape(-1, 8 if n % 8 == 0 else 1), rng.random(n).reshape(-1, 8 if n % 8 == 0 else 1), E)
 
 
 def test_empty_batch(moe):
