@@ -115,11 +115,13 @@ int moe_prepare_weight_scales(const void* sf, int E, int N, int K, int pairing, 
 
 /* Dispatch plan (DeepEP -> Mega MoE page, dispatch.cuh snippet: expert count,
  * prefix sum, slot assignment; Dispatch/Combine page section 3.1).
- * Enqueues three kernels: per-chunk expert histograms (warp-aggregated
- * shared-memory atomics), a prefix sum over chunks and experts (offsets,
+ * Computes per-chunk expert histograms (2048 entries a chunk; warp-aggregated
+ * shared-memory atomics), prefix sums over chunks and experts (offsets,
  * row-block-padded offsets, the tile table), and a stable slot per entry:
  * slot = padded offset of its expert + number of earlier (smaller flat index
- * t*k+j) entries of the same expert.  Entries with id -1 are skipped; ids
+ * t*k+j) entries of the same expert.  Enqueues a memset of the workspace's
+ * error region and ONE kernel for E <= 256 (or E > 256 with T*k <= 2048),
+ * otherwise three kernels; none of them needs its CTAs to be co-resident.  Entries with id -1 are skipped; ids
  * outside [-1, E) are skipped and flagged (MOE_ERR_BAD_EXPERT_ID, via
  * moe_plan_check).
  *   plan       out (host): filled on success
