@@ -8,21 +8,21 @@
 // The pages assign slots with a global atomicAdd, so the order of tokens
 // inside an expert is not reproducible.  Here the slot of entry i = t*k+j is
 // its expert's padded offset plus the number of entries of the same expert
-// with a smaller flat index -- a stable counting sort -- computed with three
-// kernels and no atomics on the result:
-//   route_count  one CTA per chunk of kRouteChunk entries: shared-memory
-//                histogram, warp-aggregated (one atomic per distinct expert
-//                per warp, via __match_any_sync)
-//   route_scan   one CTA: per-expert prefix over chunks, exclusive scans of
-//                counts and of counts padded to MOE_BLOCK_M, the row-block ->
-//                expert table, the number of row blocks, and the inverse maps
-//                of the padding rows (one warp per expert)
-//   route_slot   one CTA per chunk: ranks inside the chunk in flat order
-//                (rank in warp from the match mask, plus same-expert counts of
-//                lower warps), inverse maps of every routed pool row
-// A batch of at most kRouteChunk entries (decode-sized) takes one kernel
-// instead, route_small: the same three steps in one CTA, so the plan is a
-// single launch.
+// with a smaller flat index -- a stable counting sort -- with no atomics on
+// the result.  Three steps over chunks of kRouteChunk entries:
+//   count  shared-memory histogram per chunk, warp-aggregated (one atomic
+//          per distinct expert per warp, via __match_any_sync)
+//   scan   per-expert prefix over chunks, exclusive scans of counts and of
+//          counts padded to MOE_BLOCK_M, the row-block -> expert table, the
+//          number of row blocks, and the inverse maps of the padding rows
+//   slot   ranks inside each chunk in flat order (rank in warp from the match
+//          mask, plus same-expert counts of lower warps), inverse maps of
+//          every routed pool row
+// Up to kFusedMaxExperts experts the whole plan is ONE multi-CTA launch,
+// route_fused (described where it is defined).  Beyond that, a batch of at
+// most kRouteChunk entries takes one single-CTA kernel, route_small, and
+// larger ones the three kernels route_count (one CTA per chunk), route_scan
+// (one CTA) and route_slot (one CTA per chunk).
 #include <cuda_runtime.h>
 
 #include <algorithm>
