@@ -75,3 +75,24 @@ def test_argument_errors_before_any_device_call(libmoe):
     libmoe.moe_error_string.restype = ctypes.c_char_p
     for s in range(8):
         assert libmoe.moe_error_string(s)
+
+
+def test_selftest_argument_errors_without_a_device(libmoe):
+    """The calibration self-tests check their arguments before touching the
+    device: null, misaligned or out-of-range arguments are MOE_ERR_INVALID_ARG."""
+    f = libmoe.moe_selftest_stream_rate
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int),
+                                          ctypes.c_void_p]
+    ctas = ctypes.c_int(0)
+    ok = 1 << 20  # any 16-byte aligned address; never dereferenced on these paths
+    assert f(None, ok, ok, ok, 16, ok, ctypes.byref(ctas), None) == 1
+    assert f(ok, ok, ok, ok + 8, 16, ok, ctypes.byref(ctas), None) == 1   # misaligned scale pointer
+    assert f(ok, ok, ok, ok, 0, ok, ctypes.byref(ctas), None) == 1        # no k-blocks
+    assert f(ok, ok, ok, ok, (1 << 20) + 1, ok, ctypes.byref(ctas), None) == 1
+    assert f(ok, ok, ok, ok, 16, None, ctypes.byref(ctas), None) == 1     # no status word
+    g = libmoe.moe_selftest_mma_rate
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_void_p]
+    assert g(0, ok, ctypes.byref(ctas), None) == 1
+    assert g(16, None, ctypes.byref(ctas), None) == 1
