@@ -53,7 +53,9 @@ typedef enum moe_status {
     MOE_ERR_BAD_EXPERT_ID = 5, /* device saw topk_idx outside [-1, E); those entries were skipped */
     MOE_ERR_TIMEOUT = 6,       /* a bounded device-side wait expired; outputs are invalid */
     MOE_ERR_NO_KERNEL = 7,     /* the library holds no code for this device */
-    MOE_ERR_TOO_LARGE = 8      /* sizes exceed the fixed scratch of moe_expert_offsets_static() */
+    MOE_ERR_TOO_LARGE = 8,     /* sizes exceed the fixed scratch of moe_expert_offsets_static() */
+    MOE_ERR_DEBUG_BOUNDS = 9   /* debug build only (-DMOE_DEBUG): a device bounds check on a plan table
+                                  fired and the access was skipped; outputs are invalid */
 } moe_status;
 
 /* Rows of one MMA tile; every expert's pool segment is padded to a whole
@@ -231,7 +233,8 @@ int moe_forward(const void* x, const moe_weights_t* W1, const moe_weights_t* W2,
                 const moe_plan_t* plan, void* y, const moe_options_t* opts, void* stream);
 
 /* Synchronises `stream`, then returns the first device-side error recorded
- * in the plan's workspace (MOE_ERR_BAD_EXPERT_ID, MOE_ERR_TIMEOUT) or
+ * in the plan's workspace (MOE_ERR_DEBUG_BOUNDS, MOE_ERR_TIMEOUT,
+ * MOE_ERR_BAD_EXPERT_ID, in that order of precedence) or
  * MOE_OK.  The record is cleared by the next moe_plan() on that workspace. */
 int moe_plan_check(const moe_plan_t* plan, void* stream);
 

@@ -33,6 +33,7 @@ ERR_CUDA = 4
 ERR_BAD_EXPERT_ID = 5
 ERR_TIMEOUT = 6
 ERR_TOO_LARGE = 8
+ERR_DEBUG_BOUNDS = 9   # debug builds (MOE_DEBUG) only
 SF_PAIRS_ADJACENT = 0
 SF_PAIRS_HALVES = 1
 

@@ -314,6 +314,7 @@ int moe_plan_check(const moe_plan_t* plan, void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
     int err = 0;
     if (cudaMemcpy(&err, ps->ws + L.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (err & kDevErrBounds) return MOE_ERR_DEBUG_BOUNDS;
     if (err & kDevErrTimeout) return MOE_ERR_TIMEOUT;
     if (err & kDevErrBadExpert) return MOE_ERR_BAD_EXPERT_ID;
     return MOE_OK;
@@ -389,6 +390,8 @@ const char* moe_error_string(int status) {
         case MOE_ERR_BAD_EXPERT_ID: return "topk_idx held an expert id outside [-1, E); those entries were skipped";
         case MOE_ERR_TIMEOUT: return "a bounded device-side wait expired; outputs are invalid";
         case MOE_ERR_NO_KERNEL: return "no kernel image for this device";
+        case MOE_ERR_DEBUG_BOUNDS:
+            return "a bounds check of the debug build fired on a plan table (access skipped; outputs invalid)";
         case MOE_ERR_TOO_LARGE:
             return "sizes exceed the fixed scratch of moe_expert_offsets_static (T*k <= 262144, E <= 1024, "
                    "ceil(T*k/2048)*E <= 32768)";

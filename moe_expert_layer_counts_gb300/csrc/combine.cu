@@ -40,7 +40,8 @@ __device__ __forceinline__ void add8(float (&acc)[8], uint4 v) {
 template <int kChunks>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __restrict__ rows,
                                                             const int* __restrict__ slot_of, int T, int H, int k,
-                                                            uint16_t* __restrict__ y) {
+                                                            uint16_t* __restrict__ y, int64_t p_cap,
+                                                            int* __restrict__ err) {
     constexpr int kSeg = 256 * kChunks, kRows = 8 / kChunks;
     const int lane = threadIdx.x & 31;
     const int nseg = (H + kSeg - 1) / kSeg;
@@ -48,7 +49,11 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
     const int t = static_cast<int>(item / nseg);
     if (t >= T) return;
     const int seg = static_cast<int>(item % nseg);
-    const int my_slot = lane < k ? __ldg(slot_of + static_cast<size_t>(t) * k + lane) : -1;
+    int my_slot = lane < k ? __ldg(slot_of + static_cast<size_t>(t) * k + lane) : -1;
+    if (my_slot >= 0 && seg == 0 && !moe_dcheck(my_slot, 0, p_cap, err, kWhereCombine)) my_slot = -1;
+#ifdef MOE_DEBUG
+    if (my_slot >= p_cap) my_slot = -1;  // the other segments skip it too (reported once, above)
+#endif
     // the token's valid entries, bit j for entry j: only those rows are read,
     // in ascending j (the order of the sum)
     const uint32_t valid = __ballot_sync(0xffffffffu, my_slot >= 0);
@@ -104,14 +109,14 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
 }
 
 template <int kChunks>
-cudaError_t launch_combine_chunks(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s) {
+cudaError_t launch_combine_chunks(const Layout& L, uint8_t* ws, void* y, cudaStream_t s) {
     constexpr int kSeg = 256 * kChunks;
     const int nseg = (L.H + kSeg - 1) / kSeg;
     const int64_t items = static_cast<int64_t>(L.T) * nseg;
     const int64_t blocks = (items + kThreads / 32 - 1) / (kThreads / 32);
     combine_kernel<kChunks><<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
         reinterpret_cast<const uint16_t*>(ws + L.l2_out), reinterpret_cast<const int*>(ws + L.slot_of), L.T, L.H,
-        L.k, static_cast<uint16_t*>(y));
+        L.k, static_cast<uint16_t*>(y), L.p_cap, reinterpret_cast<int*>(ws + L.err));
     return cudaGetLastError();
 }
 
@@ -126,7 +131,7 @@ cudaError_t launch_combine_chunks(const Layout& L, const uint8_t* ws, void* y, c
 // 256-element segments; all 8 entries valid: 160 against 153 us).
 constexpr int64_t kSmallBatchWarps = 1024;
 
-cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s) {
+cudaError_t launch_combine(const Layout& L, uint8_t* ws, void* y, cudaStream_t s) {
     if (L.T == 0) return cudaSuccess;
     if (static_cast<int64_t>(L.T) * ((L.H + 1023) / 1024) <= kSmallBatchWarps)
         return launch_combine_chunks<1>(L, ws, y, s);

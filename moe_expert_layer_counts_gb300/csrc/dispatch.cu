@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
                                                                    const int* __restrict__ slot_of,
                                                                    uint8_t* __restrict__ pool_q,
                                                                    uint8_t* __restrict__ pool_sf, int scale_rule,
-                                                                   uint8_t* __restrict__ x_q) {
+                                                                   uint8_t* __restrict__ x_q, int64_t p_cap,
+                                                                   int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
     const int nseg = (H + kSeg - 1) / kSeg;
     const int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_quant_kernel(const uint16_t
         for (int j = 0; j < k; ++j) {
             const int r = __shfl_sync(0xffffffffu, my_slot, j);
             if (r < 0) continue;
+            if (!moe_dcheck(r, 0, p_cap, err, kWhereDispatch)) continue;
             if (active) {
                 if (!x_q) *reinterpret_cast<uint4*>(pool_q + static_cast<size_t>(r) * H + col) = codes;
                 if ((lane & 7) == 0) {
@@ -108,7 +110,8 @@ cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int sca
     const int64_t blocks = (items + kThreads / 32 - 1) / (kThreads / 32);
     dispatch_quant_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, s>>>(
         static_cast<const uint16_t*>(x), L.T, L.H, L.k, reinterpret_cast<const int*>(ws + L.slot_of),
-        ws + L.pool_q, ws + L.pool_sf, scale_rule, gather ? ws + L.x_q : nullptr);
+        ws + L.pool_q, ws + L.pool_sf, scale_rule, gather ? ws + L.x_q : nullptr, L.p_cap,
+        reinterpret_cast<int*>(ws + L.err));
     return cudaGetLastError();
 }
 

@@ -129,6 +129,7 @@ struct GemmParams {
     const int* max_count;   // largest expert count (plan): selects the ring shape
     const uint8_t* a_rows;  // A operand rows (pool or h), K bytes each
     int a_gather;           // layer 1: A rows gathered by token (tile::gather4 from maps.gather)
+    int E;                  // experts (the range of block_expert; checked in debug builds)
 };
 
 // Work items are handed out by a global counter (dynamic scheduling: a CTA
@@ -533,6 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
         int layer, b, j;
         decode_item<kMode>(ka, w, n_work1, layer, b, j);
         int e = __ldg(p0.block_expert + b), rows = __ldg(p0.block_rows + b);
+        // debug builds: a plan table out of range is reported and clamped, so
+        // no copy leaves its tensor (release builds trust the plan kernel)
+        if (!moe_dcheck(e, 0, p0.E, p0.err, kWhereExpertBlock)) e = 0;
+        if (!moe_dcheck(rows, 1, kBlockM + 1, p0.err, kWhereExpertBlock)) rows = kBlockM;
         bool all_l1_done = false;  // fused: every row block's layer-1 tiles seen complete
         ok = bcast(leader ? put_item(sh, seq, w, p0.err) : true);
         ++seq;
@@ -550,6 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
                 decode_item<kMode>(ka, wn, n_work1, next_layer, next_b, next_j);
                 next_e = __ldg(p0.block_expert + next_b);
                 next_rows = __ldg(p0.block_rows + next_b);
+                if (!moe_dcheck(next_e, 0, p0.E, p0.err, kWhereExpertBlock)) next_e = 0;
+                if (!moe_dcheck(next_rows, 1, kBlockM + 1, p0.err, kWhereExpertBlock)) next_rows = kBlockM;
             }
             const GemmParams& P = ka.p[layer - 1];
             const int kb_count = P.K / kBlockK;
@@ -920,6 +927,7 @@ bool fill_layer(int layer, const Layout& L, uint8_t* ws, const GemmLaunch& g, Ke
     p.sfb = static_cast<const uint8_t*>(g.w_sf);
     p.K = g.K;
     p.N = g.N;
+    p.E = L.E;
     p.I = L.I;
     p.H = L.H;
     p.err = reinterpret_cast<int*>(ws + L.err);

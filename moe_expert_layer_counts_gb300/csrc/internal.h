@@ -23,6 +23,29 @@ constexpr int kSchedWords = 4;         // work counters at the head of the sched
 // where a bounded wait expired.
 constexpr int kDevErrBadExpert = 1;
 constexpr int kDevErrTimeout = 2;
+constexpr int kDevErrBounds = 4;  // a bounds check of a debug build fired (MOE_DEBUG)
+
+// Bounds checks of debug builds (compiled with -DMOE_DEBUG; the release build
+// has none and no cost).  moe_dcheck(v, lo, hi, err, where) is true when
+// lo <= v < hi; otherwise it records kDevErrBounds in err[0] and, if no
+// earlier failure is recorded, 200 + where in err[1], and returns false so
+// the caller skips (or clamps) the access.  Places: 1 dispatch (pool row of
+// a slot), 2 combine (L2 row of a slot), 3 expert kernel (a row block's
+// expert and valid rows).
+constexpr int kWhereDispatch = 1, kWhereCombine = 2, kWhereExpertBlock = 3;
+#if defined(__CUDACC__)
+__device__ __forceinline__ bool moe_dcheck(int64_t v, int64_t lo, int64_t hi, int* err, int where) {
+#ifdef MOE_DEBUG
+    if (v >= lo && v < hi) return true;
+    atomicOr(err, kDevErrBounds);
+    atomicCAS(err + 1, 0, 200 + where);
+    return false;
+#else
+    (void)v, (void)lo, (void)hi, (void)err, (void)where;
+    return true;
+#endif
+}
+#endif
 // The error record's region: words 0-1 the record, words 4-7 the scheduling
 // words of the one-launch plan kernel (zeroed together before each plan).
 constexpr int kErrWords = 8;
@@ -61,7 +84,7 @@ cudaError_t launch_route(const Layout& L, uint8_t* ws, const int64_t* topk_idx, 
 // (the pool's scales are written either way).
 cudaError_t launch_dispatch(const Layout& L, uint8_t* ws, const void* x, int scale_rule, bool gather,
                             cudaStream_t s);
-cudaError_t launch_combine(const Layout& L, const uint8_t* ws, void* y, cudaStream_t s);
+cudaError_t launch_combine(const Layout& L, uint8_t* ws, void* y, cudaStream_t s);
 cudaError_t launch_prepare_sf(const uint8_t* sf, int E, int N, int K, int halves, uint8_t* out, size_t out_bytes,
                               cudaStream_t s);
 

@@ -96,3 +96,14 @@ def test_selftest_argument_errors_without_a_device(libmoe):
     g.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.c_void_p]
     assert g(0, ok, ctypes.byref(ctas), None) == 1
     assert g(16, None, ctypes.byref(ctas), None) == 1
+
+
+def test_debug_build_exports_the_same_symbols():
+    """The MOE_DEBUG variant (device bounds checks on plan tables) builds for
+    sm_103a and exports exactly what include/moe.h declares."""
+    from moe_expert_layer_counts_gb300 import build as b
+    lib = ctypes.CDLL(b.build(debug=True))
+    for n in header_functions():
+        assert hasattr(lib, n), n
+    lib.moe_error_string.restype = ctypes.c_char_p
+    assert b"debug" in lib.moe_error_string(9)
