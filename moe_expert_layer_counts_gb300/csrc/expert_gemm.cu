@@ -31,6 +31,7 @@
 // Every wait is bounded (a global-timer deadline); on expiry the CTA records
 // an error in the workspace, waits for its own copies in flight, releases
 // tensor memory and exits.
+#include <atomic>
 #include <limits>
 
 #include <cuda.h>
@@ -819,15 +820,20 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Looked up once; concurrent first calls from several host threads look it up
+// alike and store the same pointer.
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
+    static std::atomic<EncodeTiledFn> cached{nullptr};
+    EncodeTiledFn fn = cached.load(std::memory_order_acquire);
     if (!fn) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+            q == cudaDriverEntryPointSuccess) {
             fn = reinterpret_cast<EncodeTiledFn>(p);
+            cached.store(fn, std::memory_order_release);
+        }
     }
     return fn;
 }
@@ -899,16 +905,17 @@ bool make_layer1_operand_maps(CUtensorMap* a_map, const void* a, CUtensorMap* b_
 
 namespace {
 
-// Opt a kernel into its dynamic shared memory once per device.
+// Opt a kernel into its dynamic shared memory once per device (a repeated
+// call from another host thread sets the same attribute again, harmlessly).
 template <typename Kernel>
 cudaError_t smem_attr_once(Kernel kernel, int slot, int bytes) {
-    static int done[9][64] = {};
+    static std::atomic<int> done[9][64] = {};
     int dev = 0;
     cudaError_t st = cudaGetDevice(&dev);
     if (st != cudaSuccess) return st;
-    if (dev < 64 && done[slot][dev]) return cudaSuccess;
+    if (dev < 64 && done[slot][dev].load(std::memory_order_acquire)) return cudaSuccess;
     st = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (st == cudaSuccess && dev < 64) done[slot][dev] = 1;
+    if (st == cudaSuccess && dev < 64) done[slot][dev].store(1, std::memory_order_release);
     return st;
 }
 

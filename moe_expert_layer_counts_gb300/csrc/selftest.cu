@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -254,15 +256,15 @@ __global__ void __launch_bounds__(96, 1) stream_rate_kernel(const __grid_constan
 
 cudaError_t launch_stream_rate_selftest(const void* a, const void* b, const void* sfa, const void* sfb, int kblocks,
                                         int ctas, int32_t* status, cudaStream_t s) {
-    static int attr_done[64] = {};
+    static std::atomic<int> attr_done[64] = {};
     int dev = 0;
     cudaError_t st = cudaGetDevice(&dev);
     if (st != cudaSuccess) return st;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         st = cudaFuncSetAttribute(stream_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStrSmem);
         if (st != cudaSuccess) return st;
-        attr_done[dev] = 1;
+        attr_done[dev].store(1, std::memory_order_release);
     }
     StreamMaps m;
     if (!make_layer1_operand_maps(&m.a, a, &m.b, b, kStrK, kStrRows)) return cudaErrorInvalidValue;
@@ -273,15 +275,15 @@ cudaError_t launch_stream_rate_selftest(const void* a, const void* b, const void
 }
 
 cudaError_t launch_mma_rate_selftest(int kblocks, int ctas, int32_t* status, cudaStream_t s) {
-    static int attr_done[64] = {};
+    static std::atomic<int> attr_done[64] = {};
     int dev = 0;
     cudaError_t st = cudaGetDevice(&dev);
     if (st != cudaSuccess) return st;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
         st = cudaFuncSetAttribute(mma_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);
         if (st != cudaSuccess) return st;
-        attr_done[dev] = 1;
+        attr_done[dev].store(1, std::memory_order_release);
     }
     if ((st = cudaMemsetAsync(status, 0, sizeof(int32_t), s)) != cudaSuccess) return st;
     mma_rate_kernel<<<ctas, 64, kRateSmem, s>>>(kblocks, status);
