@@ -407,7 +407,7 @@ struct KernelArgs {
     GemmParams p[2];
     int* l1_done;            // fused: per pool row block, epilogue warps done with its h rows
     int* blocks_done;        // fused: row blocks whose layer-1 tiles are all done
-    int* work_ctr;           // items handed out beyond the first gridDim.x (zero at launch)
+    int* work_ctr;           // items handed out (zero at launch)
 };
 
 // Work item w -> (layer, pool row block, tile).  kMode 1 or 2: that layer's
@@ -526,25 +526,32 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemm_kernel(const __grid_c
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok;
-        // Item numbers: the first is blockIdx.x, every later one comes from the
-        // work counter when the previous one starts, so the block metadata of
-        // the next item is loaded one item ahead and its latency never stalls
-        // the stream of copies at a tile boundary.
+        // Item numbers all come from the work counter, the first one too, so an
+        // item is only ever held by a running CTA: a layer-2 tile's wait on
+        // layer-1 tiles of lower numbers ends even when not every CTA of the
+        // launch is resident (another stream's kernels on some SMs).  The next
+        // item is taken when the current one starts, so its block metadata is
+        // loaded one item ahead and never stalls the copies at a tile boundary.
         int seq = 0;
-        int w = blockIdx.x;
-        int layer, b, j;
-        decode_item<kMode>(ka, w, n_work1, layer, b, j);
-        int e = __ldg(p0.block_expert + b), rows = __ldg(p0.block_rows + b);
-        // debug builds: a plan table out of range is reported and clamped, so
-        // no copy leaves its tensor (release builds trust the plan kernel)
-        if (!moe_dcheck(e, 0, p0.E, p0.err, kWhereExpertBlock)) e = 0;
-        if (!moe_dcheck(rows, 1, kBlockM + 1, p0.err, kWhereExpertBlock)) rows = kBlockM;
+        int w = 0;
+        if (leader) w = min(n_work, atomicAdd(ka.work_ctr, 1));
+        w = bcast(w);
+        int layer = 1, b = 0, j = 0, e = 0, rows = kBlockM;
+        if (w < n_work) {
+            decode_item<kMode>(ka, w, n_work1, layer, b, j);
+            e = __ldg(p0.block_expert + b);
+            rows = __ldg(p0.block_rows + b);
+            // debug builds: a plan table out of range is reported and clamped, so
+            // no copy leaves its tensor (release builds trust the plan kernel)
+            if (!moe_dcheck(e, 0, p0.E, p0.err, kWhereExpertBlock)) e = 0;
+            if (!moe_dcheck(rows, 1, kBlockM + 1, p0.err, kWhereExpertBlock)) rows = kBlockM;
+        }
         bool all_l1_done = false;  // fused: every row block's layer-1 tiles seen complete
         ok = bcast(leader ? put_item(sh, seq, w, p0.err) : true);
         ++seq;
-        while (ok) {
+        while (ok && w < n_work) {
             int wn = 0;
-            if (leader) wn = min(n_work, static_cast<int>(gridDim.x) + atomicAdd(ka.work_ctr, 1));
+            if (leader) wn = min(n_work, atomicAdd(ka.work_ctr, 1));
             wn = bcast(wn);
             if (!bcast(leader ? put_item(sh, seq, wn, p0.err) : true)) {
                 ok = false;
