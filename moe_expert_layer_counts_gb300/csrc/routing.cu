@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(kScanThreads) route_fused_kernel(
         const int64_t end = min(base + kRouteChunk, n_entries);
 #pragma unroll
         for (int q = 0; q < kFusedPer; ++q) {
+            if (base + q * kScanThreads >= end) break;  // a short last chunk has fewer rounds (uniform)
             const int64_t i = base + q * kScanThreads + tid;
             const int slot = rank_round(e_r[q], E, s_next, s_wcnt);
             if (i < end) write_slot(i, slot, w_r[q], k, slot_of, row_token, row_topk, row_weight);
