@@ -37,7 +37,7 @@ def _ragged_case():
     return w, idx, tw
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid", "ragged", "decode"])
+@pytest.mark.parametrize("name", ["tiny", "mid", "ragged", "decode", "share", "full"])
 def test_fused_equals_two_launches(moe, name):
     """h codes, h scales and the bf16 L2 rows of every routed pool row are
     bit-identical between moe_expert_fused and moe_expert_l1 + moe_expert_l2
