@@ -254,7 +254,7 @@ __device__ __forceinline__ void write_slot(int64_t i, int slot, float w, int k, 
 // Stable slots of chunk `chunk`: ranks inside the chunk in flat order on top
 // of s_next[e] (the expert's padded offset plus the chunk's base, set by the
 // caller, with s_wcnt zeroed); inverse maps of every routed pool row.
-// s_wcnt: [warps][E] same-expert counts per warp, this round.
+// s_wcnt: [warps][E] same-expert counts per warp of the entries being ranked.
 __device__ __forceinline__ void slot_rank(const int64_t* __restrict__ topk_idx, const float* __restrict__ topk_w,
                                           int64_t n_entries, int k, int E, int chunk, int* s_next, int* s_wcnt,
                                           int* __restrict__ slot_of, int* __restrict__ row_token,
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kSmallMaxThreads) route_small_kernel(
     extern __shared__ int s_mem[];
     const int nthreads = blockDim.x, nwarps = nthreads / 32;
     int* s_cnt = s_mem;                      // [E] counts, later the next free slot of each expert
-    int* s_wcnt = s_mem + E;                 // [nwarps][E] same-expert counts per warp, this round
+    int* s_wcnt = s_mem + E;                 // [nwarps][E] same-expert counts per warp of the entries being ranked
     int* s_pad = s_mem + E * (1 + nwarps);   // [2][E] padding rows [begin, end) of each expert
     __shared__ int s_warp[32];
     __shared__ int s_max, s_bad;
