@@ -46,6 +46,9 @@ FUSED_PLAN_EXPERTS = 256  # experts up to which the plan is one multi-CTA launch
 FLUSH_BYTES = 512 << 20
 # FLOPs of one oracle sample (about 7 s on 16 host cores at the full layer size)
 ORACLE_SAMPLE_FLOP = 4.0e11
+# the reference arm's whole run (warm-up + timed calls) stays within about this much
+# oracle work (a few minutes on 16 host cores): many steps take smaller samples
+REFERENCE_RUN_FLOP = 1.2e13
 
 
 def kernels_per_step(w, fused=True) -> int:
@@ -164,13 +167,12 @@ def measured_traffic(workload: str):
 
 
 # ------------------------------------------------------------------ oracle legs
-def oracle_sample(w):
+def oracle_sample(w, flop=ORACLE_SAMPLE_FLOP):
     """The token sample both oracle timings (cpu_baseline and the reference
-    arm) use: evenly spaced tokens, as many as make about ORACLE_SAMPLE_FLOP
-    of layer work at k entries per token (all tokens of the small
-    workloads)."""
+    arm) use: evenly spaced tokens, as many as make about `flop` of layer
+    work at k entries per token (all tokens of the small workloads)."""
     import numpy as np
-    n = min(w.T, max(32, int(ORACLE_SAMPLE_FLOP / (6.0 * w.H * w.I * w.k))))
+    n = min(w.T, max(32, int(flop / (6.0 * w.H * w.I * w.k))))
     step = max(1, w.T // n)
     return np.arange(0, w.T, step, dtype=np.int32)[:n], step
 
@@ -214,7 +216,9 @@ def run_reference(args, w, rank, world):
     oracle.build()
     d = inputs.make_inputs(w, device="cpu", weight_device="cuda" if torch.cuda.is_available() else "cpu")
     x, idx, tw, ws = _oracle_args(d)
-    toks, step = oracle_sample(w)
+    # the cpu_baseline sample unless the run's step count would make the whole
+    # run take more than a few minutes
+    toks, step = oracle_sample(w, min(ORACLE_SAMPLE_FLOP, REFERENCE_RUN_FLOP / (args.warmup + args.steps)))
     n_valid = int((idx[toks] >= 0).sum())
     times = []
     for s in range(args.warmup + args.steps):
