@@ -35,6 +35,37 @@ def test_dispatch_pool_bit_exact(moe, oracle, name):
     np.testing.assert_array_equal(sf[rows], xsf[toks])
 
 
+@pytest.mark.parametrize("rule", [0, 1])
+def test_dispatch_pool_bit_exact_at_extreme_magnitudes(moe, oracle, rule):
+    """Token rows scaled by 2^s for s from -140 to +120 (bf16 subnormals, the
+    ends of the UE8M0 range where the scale exponent clamps, exact zeros,
+    single huge or tiny values inside a block): pool codes and scale bytes
+    equal the oracle's under both scale rules."""
+    w = inputs.Workload("extreme", 96, 1024, 128, 4, 2, "uniform")
+    x = inputs.make_x(w.T, w.H, 5, "cpu").float()
+    s = torch.linspace(-140, 120, w.T).round()
+    x = x * torch.exp2(s)[:, None]
+    x[3] = 0.0                                   # an all-zero row
+    x[7, :32] = 0.0                              # an all-zero block
+    x[11, 5] = 3.0e38                            # one huge value among ordinary ones
+    x[13, 40] = 1.0e-40                          # one bf16 subnormal among ordinary ones
+    x[17] = x[17] * 0 + torch.where(torch.arange(w.H) % 2 == 0, 1.0e-38, -1.0e-39)
+    d = dict(x=x.to(torch.bfloat16).cuda())
+    d["topk_idx"], d["topk_w"] = (t.cuda() for t in inputs.make_routing(w, 1))
+    p = moe.plan(d["topk_idx"], d["topk_w"], w.E, w.H, w.I)
+    moe.dispatch(p, d["x"], options=moe.Options(scale_rule=rule))
+    assert moe.plan_check(p) == 0
+    xq, xsf = oracle.quant_x(gh.bits(d["x"]), scale_rule=rule)
+    row_token = p.export("row_token").cpu().numpy()
+    P = int(p.export("poff").cpu().numpy()[-1])
+    rows = np.nonzero(row_token[:P] >= 0)[0]
+    toks = row_token[rows]
+    pool = p.export("pool_q").cpu().numpy().reshape(-1, w.H)
+    np.testing.assert_array_equal(pool[rows], xq[toks])
+    sf = gh.sf_rows_from_mma(p.export("pool_sf").cpu().numpy(), p.export("pool_rows"), w.H)
+    np.testing.assert_array_equal(sf[rows], xsf[toks])
+
+
 def _deq_e4m3(codes, sf):
     tab = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
     v = tab[codes.astype(np.int64)]
