@@ -12,7 +12,9 @@
 // only the rows of the token's valid entries (a bit mask of them, taken in
 // ascending j), 8 / chunks rows per round with all their chunks loaded before
 // they are added, so a warp keeps 8 loads in flight whether the token has one
-// valid entry (an expert-parallel shard) or all k.
+// valid entry (an expert-parallel shard) or all k.  The L2 rows are read and y
+// is written with streaming cache hints (each byte is touched once): full
+// workload 160 -> 153 us, mid 24.6 -> 20.6 us.
 #include <cuda_runtime.h>
 
 #include "formats.cuh"
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
 #pragma unroll
             for (int c = 0; c < kChunks; ++c) {
                 v[q][c] = make_uint4(0, 0, 0, 0);
-                if (has[q] && active[c]) v[q][c] = __ldg(reinterpret_cast<const uint4*>(r[q] + c * 256));
+                if (has[q] && active[c]) v[q][c] = __ldcs(reinterpret_cast<const uint4*>(r[q] + c * 256));
             }
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const uint16_t* __res
             o.y = bf16x2_rn(acc[c][2], acc[c][3]);
             o.z = bf16x2_rn(acc[c][4], acc[c][5]);
             o.w = bf16x2_rn(acc[c][6], acc[c][7]);
-            *reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + base + c * 256) = o;
+            __stcs(reinterpret_cast<uint4*>(y + static_cast<size_t>(t) * H + base + c * 256), o);
         }
     }
 }
